@@ -1,0 +1,299 @@
+"""CPU oracle for the DSA indexer path: key store, score, causal mask, top-k.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this package.  It shares no code with the CUDA
+library and never imports it; the two see the same inputs only through the
+seeded generators in ``sparse_attention_top_idx_gb300.workloads``.
+
+The arithmetic lives in ``orc.c`` (plain C, compiled with gcc on first use);
+this module only marshals numpy arrays.  What each function follows:
+
+* e4m3 encode/decode and the per-row fp8 quantisation -- the OCP 8-bit float
+  format (e4m3, no infinities, max 448) and the 132-byte fp8 token record of
+  "The Pivot: A Single Edit That Finally Fixed DeepSeek V4's Long-Context
+  Recall Failure", section "Assumptions and Input Knowledge" (128 codes + a
+  4-byte scale; bf16 records are 256 bytes).
+* the paged store and gather -- "DeepSeek-V4 index_topk=1024 sparse indexer
+  can't recall verbatim lines" (ROCm/ATOM issue #1507), section "How it was
+  isolated" (quantise-and-cache write, gather read, block sizes 32 and 64).
+* the score sum_h w[t,h] * ReLU(q[t,h] . k[s]) in fp32 and the top-k --
+  "The Hypothesis That Refused to Die", section "The Context" (top-K over
+  compressed query-key dot products) and the ATOM issue, same section
+  (per-row top-k, index_topk 512/1024).
+
+Parity pins for every function live in ``tests/test_oracle_*.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "orc.c")
+_SO = os.path.join(_HERE, "liborc.so")
+_lock = threading.Lock()
+_handle = None
+
+FP8 = 0
+BF16 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile orc.c into liborc.so next to it (gcc, OpenMP when available)."""
+    if (not force and os.path.exists(_SO)
+            and os.path.getmtime(_SO) >= os.path.getmtime(_SRC)):
+        return _SO
+    tmp = _SO + ".tmp.%d" % os.getpid()
+    base = ["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-std=c99",
+            "-D_DEFAULT_SOURCE", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:5] + ["-fopenmp"] + base[5:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+class Oracle:
+    """The oracle bound to one compiled copy of orc.c (the default is liborc.so;
+    tests may load a deliberately altered copy to check that the pins catch it)."""
+
+    def __init__(self, so_path: str):
+        L = ctypes.CDLL(so_path)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        I = ctypes.c_int
+        L.orc_e4m3_encode_n.argtypes = [P, P, I64]
+        L.orc_e4m3_decode_n.argtypes = [P, P, I64]
+        L.orc_quant_rows.argtypes = [P, I64, I, P, P]
+        L.orc_block_bytes.argtypes = [I, I, I]
+        L.orc_block_bytes.restype = I64
+        L.orc_store_keys.argtypes = [P, I64, I, I, I, P, P, I64]
+        L.orc_store_keys.restype = I64
+        L.orc_gather_keys.argtypes = [P, I, I, I, P, I64, P, P, P]
+        L.orc_scores_row.argtypes = [I, I, I, P, P, I64, P, P, P, P, P]
+        L.orc_topk_row.argtypes = [P, I64, I, P, P]
+        L.orc_score_topk.argtypes = [I, I, I, I, I64, P, P, P, P, P, P, P, P,
+                                     P, P, I64, P, P]
+        L.orc_num_threads.restype = I
+        L.orc_set_num_threads.argtypes = [I]
+        self.L = L
+
+    def num_threads(self) -> int:
+        return int(self.L.orc_num_threads())
+
+
+    def set_num_threads(self, n: int) -> None:
+        self.L.orc_set_num_threads(int(n))
+
+
+    # --------------------------------------------------------------------------
+    # fp8 e4m3
+    # --------------------------------------------------------------------------
+
+    def e4m3_encode(self, x) -> np.ndarray:
+        """fp32 -> e4m3 code, round-to-nearest-even, saturating, NaN -> 0x7F."""
+        x = _c(x, np.float32)
+        out = np.empty(x.shape, np.uint8)
+        self.L.orc_e4m3_encode_n(_p(x), _p(out), x.size)
+        return out
+
+
+    def e4m3_decode(self, codes) -> np.ndarray:
+        """e4m3 code -> its fp32 value (NaN for S.1111.111)."""
+        c = _c(codes, np.uint8)
+        out = np.empty(c.shape, np.float32)
+        self.L.orc_e4m3_decode_n(_p(c), _p(out), c.size)
+        return out
+
+
+    def bf16_to_f32(self, bits) -> np.ndarray:
+        """bf16 bit patterns (uint16) -> fp32 values (exact: the bits shifted up)."""
+        b = _c(bits, np.uint16)
+        return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+    def quantize_rows(self, x_bf16):
+        """Per-row fp8 quantisation of bf16 rows [R, d] -> (codes [R, d], scales [R])."""
+        x = _c(x_bf16, np.uint16)
+        R, d = x.shape
+        codes = np.empty((R, d), np.uint8)
+        scales = np.empty(R, np.float32)
+        self.L.orc_quant_rows(_p(x), R, d, _p(codes), _p(scales))
+        return codes, scales
+
+
+    # --------------------------------------------------------------------------
+    # paged cache
+    # --------------------------------------------------------------------------
+
+    def block_bytes(self, dtype: int, bs: int, d: int = 128) -> int:
+        return int(self.L.orc_block_bytes(dtype, bs, d))
+
+
+    def store_keys(self, pool: np.ndarray, k_bf16, slot_mapping, bs: int, dtype: int) -> int:
+        """Write keys into a flat uint8 pool in place; returns tokens written."""
+        assert pool.dtype == np.uint8 and pool.flags.c_contiguous
+        k = _c(k_bf16, np.uint16)
+        sm = _c(slot_mapping, np.int64)
+        n, d = k.shape
+        bb = self.block_bytes(dtype, bs, d)
+        nb = pool.size // bb
+        r = self.L.orc_store_keys(_p(pool), nb, bs, d, dtype, _p(k), _p(sm), n)
+        if r < 0:
+            raise ValueError("slot out of range")
+        return int(r)
+
+
+    def gather_keys(self, pool: np.ndarray, table_row, S: int, bs: int, dtype: int, d: int = 128):
+        """Read the first S logical keys of a sequence back out of the pool."""
+        t = _c(table_row, np.int32)
+        if dtype == FP8:
+            codes = np.empty((S, d), np.uint8)
+            scales = np.empty(S, np.float32)
+            self.L.orc_gather_keys(_p(pool), bs, d, dtype, _p(t), S, _p(codes), _p(scales), None)
+            return codes, scales
+        kb = np.empty((S, d), np.uint16)
+        self.L.orc_gather_keys(_p(pool), bs, d, dtype, _p(t), S, None, None, _p(kb))
+        return kb
+
+
+    # --------------------------------------------------------------------------
+    # scores and top-k
+    # --------------------------------------------------------------------------
+
+    def scores_row(self, dtype: int, q_bf16, w, keys, nvis: int, exact: bool = False):
+        """Scores of one query row q [H, d] (bf16 bits) against the first nvis keys.
+
+        keys: (codes [S, d] uint8, scales [S] fp32) for fp8, or bf16 bits [S, d].
+        Returns fp32 scores [nvis] (and the fp64 evaluation when exact=True).
+        """
+        q = _c(q_bf16, np.uint16)
+        H, d = q.shape
+        w = _c(w, np.float32)
+        out = np.empty(max(nvis, 0), np.float32)
+        ex = np.empty(max(nvis, 0), np.float64) if exact else None
+        if dtype == FP8:
+            kc, ks = _c(keys[0], np.uint8), _c(keys[1], np.float32)
+            self.L.orc_scores_row(dtype, d, H, _p(q), _p(w), nvis, _p(kc), _p(ks), None,
+                                  _p(out), _p(ex))
+        else:
+            kb = _c(keys, np.uint16)
+            self.L.orc_scores_row(dtype, d, H, _p(q), _p(w), nvis, None, None, _p(kb),
+                                  _p(out), _p(ex))
+        return (out, ex) if exact else out
+
+
+    def topk_row(self, scores, k: int):
+        """Top-k of a score row: (idx [k] int32, score [k] fp32), -1 / -inf padded."""
+        s = _c(scores, np.float32)
+        idx = np.empty(k, np.int32)
+        sc = np.empty(k, np.float32)
+        self.L.orc_topk_row(_p(s), s.size, k, _p(idx), _p(sc))
+        return idx, sc
+
+
+    def score_topk(self, dtype: int, k: int, q_bf16, w, row_seq, row_pos, seq_keys,
+                   full_scores: bool = False, exact: bool = False):
+        """The whole path for R query rows.
+
+        q_bf16: [R, H, d] bf16 bits; w: [R, H] fp32.
+        row_seq[r]: the sequence of row r; row_pos[r]: its position (sees 0..pos).
+        seq_keys: list over sequences of logical keys, (codes, scales) for fp8 or
+        bf16 bits [S, d] for bf16.
+        Returns dict(idx [R, k], score [R, k], and optionally scores [R, max_s]
+        (NaN where not visible) and exact [R, max_s]).
+        """
+        q = _c(q_bf16, np.uint16)
+        R, H, d = q.shape
+        w = _c(w, np.float32).reshape(R, H)
+        row_seq = _c(row_seq, np.int32)
+        row_pos = _c(row_pos, np.int64)
+        lens = [(kk[0].shape[0] if dtype == FP8 else kk.shape[0]) for kk in seq_keys]
+        key_off = np.zeros(len(lens), np.int64)
+        if len(lens) > 1:
+            key_off[1:] = np.cumsum(lens)[:-1]
+        assert np.all(row_pos < np.asarray(lens, np.int64)[row_seq])
+        if dtype == FP8:
+            kc = _c(np.concatenate([kk[0] for kk in seq_keys]) if lens else
+                    np.zeros((0, d), np.uint8), np.uint8)
+            ks = _c(np.concatenate([kk[1] for kk in seq_keys]) if lens else
+                    np.zeros(0, np.float32), np.float32)
+            kb = None
+        else:
+            kc = ks = None
+            kb = _c(np.concatenate(seq_keys) if lens else np.zeros((0, d), np.uint16), np.uint16)
+        idx = np.empty((R, k), np.int32)
+        sc = np.empty((R, k), np.float32)
+        max_s = int(max(row_pos.max() + 1, 1)) if R else 1
+        full = np.full((R, max_s), np.nan, np.float32) if full_scores else None
+        exf = np.full((R, max_s), np.nan, np.float64) if exact else None
+        self.L.orc_score_topk(dtype, d, H, k, R, _p(q), _p(w), _p(row_seq), _p(row_pos),
+                              _p(key_off), _p(kc), _p(ks), _p(kb), _p(idx), _p(sc),
+                              max_s, _p(full), _p(exf))
+        out = {"idx": idx, "score": sc}
+        if full_scores:
+            out["scores"] = full
+        if exact:
+            out["exact"] = exf
+        return out
+
+
+
+
+def _default() -> Oracle:
+    global _handle
+    with _lock:
+        if _handle is None:
+            _handle = Oracle(build())
+        return _handle
+
+
+def load_variant(so_path: str) -> Oracle:
+    """Load another compiled copy of orc.c (used by the pin tests)."""
+    return Oracle(so_path)
+
+
+def __getattr__(name):
+    # Module-level access (oracle.score_topk, ...) goes to the default build.
+    if name.startswith("_"):
+        raise AttributeError(name)
+    return getattr(_default(), name)
+
+
+# --------------------------------------------------------------------------
+# reports used with the synthetic needle test
+# --------------------------------------------------------------------------
+
+def needle_rank(scores, needle: int) -> int:
+    """1 + the number of keys scoring strictly above the needle."""
+    s = np.asarray(scores)
+    return 1 + int(np.sum(s > s[needle]))
+
+
+def jaccard(a, b) -> float:
+    """|A & B| / |A | B| over the valid (>= 0) indices of two top-k lists."""
+    A = set(int(x) for x in np.asarray(a).ravel() if x >= 0)
+    B = set(int(x) for x in np.asarray(b).ravel() if x >= 0)
+    u = A | B
+    return len(A & B) / len(u) if u else 1.0
+
+
+def lost(a_ref, b) -> int:
+    """Positions of the reference top-k that the other list dropped."""
+    A = set(int(x) for x in np.asarray(a_ref).ravel() if x >= 0)
+    B = set(int(x) for x in np.asarray(b).ravel() if x >= 0)
+    return len(A - B)
