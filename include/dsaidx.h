@@ -1,0 +1,208 @@
+/*
+ * dsaidx.h -- C ABI of the DSA lightning-indexer library for GB300 (sm_103a).
+ *
+ * The library implements the indexer hot path of DeepSeek sparse attention:
+ * store per-token 128-dim index keys in a paged cache, score every causally
+ * visible key against each query and return the index_topk best positions.
+ *
+ * What the operations follow:
+ *  - "DeepSeek-V4 index_topk=1024 sparse indexer can't recall verbatim lines"
+ *    (ROCm/ATOM issue #1507), section "How it was isolated": index keys are
+ *    quantised to fp8 with a per-token scale and scattered into a paged cache
+ *    (indexer_k_quant_and_cache), scored per query straight from the paged
+ *    blocks at block size 32 or 64 (paged MQA logits), and reduced to the
+ *    index_topk best positions per row (top_k_per_row_decode); prefill scores
+ *    causal query chunks the same way (_score_topk_prefill).  Section
+ *    "Environment": index_topk 1024 (512 in the repro), contexts up to
+ *    1,048,576 tokens.
+ *  - "The Pivot: A Single Edit That Finally Fixed DeepSeek V4's Long-Context
+ *    Recall Failure", section "Assumptions and Input Knowledge": an fp8 index
+ *    key takes 132 bytes per token (128 e4m3 codes + one fp32 scale), a bf16
+ *    key 256 bytes.
+ *  - "The Hypothesis That Refused to Die", section "The Context": the indexer
+ *    ranks every cached position by a compressed query-key dot product and
+ *    keeps the top K.  The score computed here is
+ *        score[t, s] = sum_h w[t, h] * ReLU(q[t, h] . k[s])
+ *    accumulated in fp32, with the per-head weights w supplied by the caller
+ *    (any softmax or head-count scaling is folded into w).
+ *
+ * Conventions shared by every call:
+ *  - head_dim is 128.  heads is 64 (other head counts return
+ *    IDX_ERR_UNSUPPORTED).  topk is 1..2048.
+ *  - Every pointer named *_dev is a device pointer into memory the caller owns
+ *    (the library never allocates or frees device memory and never
+ *    synchronises a stream, except idx_read_device_status).  `stream` is a
+ *    cudaStream_t passed as void* (NULL = the legacy default stream).
+ *  - Results are valid in stream order after the call's kernels complete.
+ *  - Host-side argument errors return at once, before any launch, and leave
+ *    every buffer untouched.  Problems only the device can see (a block id
+ *    outside the pool, seq_len > max_seq_len, a slot outside the pool, a
+ *    pipeline wait that ran out) set a status word in the workspace (or in
+ *    status_dev for idx_store_keys), skip the offending work and write -1 rows
+ *    for the affected queries; no kernel traps or faults on them.
+ *  - Query positions: the nq_b queries of sequence b are its LAST nq_b
+ *    positions, pos = seq_len_b - nq_b + i, and a query sees keys s <= pos.
+ *    Decode is the case nq_b = 1 (every key of the sequence is visible).
+ *  - Top-k output: indices in descending score order, equal scores ordered by
+ *    ascending index; when fewer than topk keys are visible the row is padded
+ *    with index -1 (and score -inf).
+ */
+#ifndef DSAIDX_H
+#define DSAIDX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define IDX_HEAD_DIM 128
+#define IDX_MAX_TOPK 2048
+
+typedef enum idx_status {
+    IDX_OK = 0,
+    IDX_ERR_INVALID_ARG = 1,        /* null pointer, bad size or out-of-range argument */
+    IDX_ERR_UNSUPPORTED = 2,        /* valid but not built: heads != 64, head_dim != 128 */
+    IDX_ERR_CUDA = 3,               /* a CUDA runtime call or launch failed */
+    IDX_ERR_WORKSPACE_TOO_SMALL = 4,
+    IDX_ERR_DEVICE_CHECK = 5,       /* device-side check failed (see idx_read_device_status) */
+    IDX_ERR_TIMEOUT = 6             /* a bounded device wait ran out */
+} idx_status;
+
+/* Index-key storage formats of the paged cache. */
+typedef enum idx_key_dtype {
+    IDX_KEY_FP8_E4M3 = 0,   /* 128 e4m3 codes + fp32 scale per token (132 B) */
+    IDX_KEY_BF16 = 1        /* 128 bf16 values per token (256 B) */
+} idx_key_dtype;
+
+/* Opaque host handle bound to one pool on the current device.  It holds the
+ * pool geometry and the TMA descriptors of the pool; it owns no device
+ * memory.  Not thread-safe to destroy while calls using it are being issued. */
+typedef struct idx_cache idx_cache;
+
+/*
+ * Bytes of one paged block.  Layout of an fp8 block of bs tokens: bs rows of
+ * 128 one-byte e4m3 codes (row i at byte 128*i), then bs fp32 scales (scale i
+ * at byte 128*bs + 4*i): 8448 bytes at bs = 64.  A bf16 block is bs rows of
+ * 128 bf16 values (row i at byte 256*i).  Returns 0 for unsupported arguments.
+ * Follows the 132 / 256 bytes-per-token records of "The Pivot: A Single Edit
+ * That Finally Fixed DeepSeek V4's Long-Context Recall Failure", section
+ * "Assumptions and Input Knowledge"; the in-block order of codes and scales is
+ * this library's choice (it keeps every 128-byte code row 16-byte aligned for
+ * TMA).
+ */
+size_t idx_block_bytes(int key_dtype, int block_size, int head_dim);
+
+/*
+ * Bind a caller-owned pool of num_blocks blocks to a new handle.
+ *  pool_dev: device pointer, 256-byte aligned, num_blocks * idx_block_bytes()
+ *            bytes.  block_size: 32 or 64 (ROCm/ATOM issue #1507, section
+ *            "How it was isolated", checks both).  head_dim: 128.
+ * Errors: IDX_ERR_INVALID_ARG (null, misaligned, num_blocks < 1 or >= 2^31,
+ * bad block size), IDX_ERR_UNSUPPORTED (head_dim), IDX_ERR_CUDA (no device or
+ * the TMA descriptor could not be built).  *out is set only on IDX_OK.
+ */
+idx_status idx_cache_create(idx_cache** out, void* pool_dev, int64_t num_blocks,
+                            int block_size, int head_dim, int key_dtype);
+
+/* Release a handle (host memory only; the pool is untouched).  NULL is a no-op. */
+void idx_cache_destroy(idx_cache* cache);
+
+/*
+ * Quantise n keys and scatter them into the pool (the quant-and-cache write of
+ * ROCm/ATOM issue #1507, section "How it was isolated").
+ *  k_bf16_dev:       [n, 128] bf16, row-major, 16-byte aligned.
+ *  slot_mapping_dev: [n] int64; token i goes to slot = block * block_size +
+ *                    offset.  A negative slot skips the token; a slot beyond
+ *                    the pool skips it too and sets status_dev.
+ *  status_dev:       nullable device int32; set to IDX_ERR_DEVICE_CHECK when a
+ *                    slot was out of range (never cleared by the library).
+ * fp8 pools: per token amax over the 128 values, scale = amax / 448 (IEEE
+ * division), code_i = e4m3(x_i / scale) rounded to nearest even with
+ * saturation to +-448; amax = 0 gives scale 0 and zero codes.  bf16 pools:
+ * the 256 bytes are copied.
+ */
+idx_status idx_store_keys(const idx_cache* cache, const void* k_bf16_dev,
+                          const int64_t* slot_mapping_dev, int64_t n,
+                          int32_t* status_dev, void* stream);
+
+/*
+ * Workspace bytes a decode call needs for this batch shape (depends on the
+ * handle's device and key format).  0 on invalid arguments.
+ */
+size_t idx_workspace_bytes_decode(const idx_cache* cache, int batch, int max_seq_len,
+                                  int heads, int topk);
+
+/*
+ * Zero a newly allocated workspace (required once before its first use, and
+ * again after any call that reported a device error).  The score calls leave
+ * the workspace ready for the next call.
+ */
+idx_status idx_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream);
+
+/*
+ * Decode: one query per sequence, every key of the sequence visible
+ * (deepgemm_fp8_paged_mqa_logits + top_k_per_row_decode in ROCm/ATOM issue
+ * #1507, section "How it was isolated", fused into one kernel: the scores stay
+ * in shared memory).
+ *  q_bf16_dev:      [batch, heads, 128] bf16.  fp8 pools: each (b, h) row is
+ *                   quantised like a key (scale sq = amax / 448) and the scale
+ *                   folded into the head weight, w' = w * sq.
+ *  w_dev:           [batch, heads] fp32 head weights.
+ *  block_table_dev: [batch, max_blocks_per_seq] int32 physical block ids;
+ *                   logical key s of sequence b lives in block
+ *                   block_table[b][s / block_size], row s % block_size.
+ *  seq_lens_dev:    [batch] int32 keys per sequence (0 allowed).
+ *  max_seq_len:     host upper bound on seq_lens (sizes the grid).
+ *  out_idx_dev:     [batch, topk] int32.  out_score_dev: nullable
+ *                   [batch, topk] fp32 scores of the selected keys.
+ *  workspace_dev:   ws_bytes >= idx_workspace_bytes_decode(...), zeroed once
+ *                   by idx_workspace_init; 256-byte aligned.
+ * Concurrent calls must not share a workspace.
+ */
+idx_status idx_score_topk_decode(const idx_cache* cache, const void* q_bf16_dev,
+                                 const float* w_dev, const int32_t* block_table_dev,
+                                 int max_blocks_per_seq, const int32_t* seq_lens_dev,
+                                 int batch, int max_seq_len, int heads, int topk,
+                                 int32_t* out_idx_dev, float* out_score_dev,
+                                 void* workspace_dev, size_t ws_bytes, void* stream);
+
+/* Workspace bytes a prefill call needs.  0 on invalid arguments. */
+size_t idx_workspace_bytes_prefill(const idx_cache* cache, int batch, int total_q,
+                                   int max_seq_len, int heads, int topk);
+
+/*
+ * Prefill: causal query chunks (_score_topk_prefill in ROCm/ATOM issue #1507,
+ * section "Root cause found", reading the paged cache directly instead of a
+ * gathered copy).
+ *  q_bf16_dev:       [total_q, heads, 128] bf16; w_dev: [total_q, heads] fp32.
+ *  cu_seqlens_q_dev: [batch + 1] int32, cu[0] = 0, rows cu[b]..cu[b+1]-1 are
+ *                    the queries of sequence b (at its last positions).
+ *  seq_lens_dev:     [batch] int32 keys of each sequence, this chunk included.
+ *  out_idx_dev:      [total_q, topk]; out_score_dev nullable [total_q, topk].
+ * Other arguments as for decode.  batch <= 4096.
+ */
+idx_status idx_score_topk_prefill(const idx_cache* cache, const void* q_bf16_dev,
+                                  const float* w_dev, const int32_t* cu_seqlens_q_dev,
+                                  const int32_t* seq_lens_dev, const int32_t* block_table_dev,
+                                  int max_blocks_per_seq, int batch, int total_q,
+                                  int max_seq_len, int heads, int topk,
+                                  int32_t* out_idx_dev, float* out_score_dev,
+                                  void* workspace_dev, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronise `stream` and read the device status word of a workspace into
+ * *code_out (IDX_OK, IDX_ERR_DEVICE_CHECK or IDX_ERR_TIMEOUT).  For tests and
+ * debugging; the status stays set until idx_workspace_init.
+ */
+idx_status idx_read_device_status(const void* workspace_dev, void* stream, int32_t* code_out);
+
+/* Static description of a status code. */
+const char* idx_status_str(idx_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSAIDX_H */

@@ -1,0 +1,107 @@
+// store.cu -- key quantise/scatter into the paged index-key cache.
+//
+// Follows the quant-and-cache write of "DeepSeek-V4 index_topk=1024 sparse
+// indexer can't recall verbatim lines" (ROCm/ATOM issue #1507, section "How it
+// was isolated": indexer_k_quant_and_cache) with the 132 / 256 bytes-per-token
+// records of "The Pivot: A Single Edit That Finally Fixed DeepSeek V4's
+// Long-Context Recall Failure" (section "Assumptions and Input Knowledge").
+//
+// One token per half-warp: each of the 16 lanes loads 16 bytes (8 bf16) of
+// the key.  fp8: the half-warp reduces amax with shuffles, divides (IEEE) by
+// the scale, converts pairs with the hardware e4m3 convert (round to nearest
+// even, saturating), pairs of lanes merge their 8 code bytes so that 8 lanes
+// write the 128-byte code row as 16-byte stores, and lane 0 writes the scale.
+// bf16: each lane copies its 16 bytes to the slot.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dsaidx {
+
+namespace {
+
+// Two fp32 values -> two e4m3 codes (lo = a, hi = b), round to nearest even,
+// finite values beyond 448 saturate.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float a, float b) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(256) store_keys_kernel(const uint4* __restrict__ k,
+                                                         const int64_t* __restrict__ slots,
+                                                         int64_t n, uint8_t* __restrict__ pool,
+                                                         int64_t num_blocks, int bs,
+                                                         int64_t block_bytes, int32_t* status) {
+    const int sub = threadIdx.x & 15;                     // lane within the half-warp
+    const unsigned hmask = 0xFFFFu << (threadIdx.x & 16);  // this half-warp's lanes
+    const int64_t tok0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+    const int64_t tstride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
+    // The trip count is uniform over a half-warp, which is all the shuffles span.
+    for (int64_t tok = tok0; tok < n; tok += tstride) {
+        const int64_t slot = slots[tok];
+        const bool neg = slot < 0;
+        const int64_t blk = neg ? 0 : slot / bs;
+        const bool oob = !neg && blk >= num_blocks;
+        if (oob && sub == 0) set_status(status, IDX_ERR_DEVICE_CHECK);
+        if (neg || oob) continue;                          // uniform over the half-warp
+        const int64_t off = slot - blk * bs;
+        uint8_t* base = pool + blk * block_bytes;
+        const uint4 v = k[tok * 16 + sub];
+        if constexpr (!kFp8) {
+            reinterpret_cast<uint4*>(base + off * 256)[sub] = v;
+        } else {
+            float x[8];
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[2 * i] = __uint_as_float(w4[i] << 16);
+                x[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(hmask, amax, o, 16));
+            const float scale = __fdiv_rn(amax, 448.0f);
+            uint32_t lo = 0, hi = 0;
+            if (amax != 0.0f) {
+                float y[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(x[i], scale);
+                lo = cvt_e4m3x2(y[0], y[1]) | (cvt_e4m3x2(y[2], y[3]) << 16);
+                hi = cvt_e4m3x2(y[4], y[5]) | (cvt_e4m3x2(y[6], y[7]) << 16);
+            }
+            // lane pairs (2j, 2j+1) -> one 16-byte store by the even lane
+            const uint32_t plo = __shfl_down_sync(hmask, lo, 1, 16);
+            const uint32_t phi = __shfl_down_sync(hmask, hi, 1, 16);
+            if ((sub & 1) == 0) {
+                uint4 o4 = make_uint4(lo, hi, plo, phi);
+                reinterpret_cast<uint4*>(base + off * 128)[sub >> 1] = o4;
+            }
+            if (sub == 0) *reinterpret_cast<float*>(base + static_cast<int64_t>(bs) * 128 + off * 4) = scale;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_store(const idx_cache* c, const void* k, const int64_t* slots, int64_t n,
+                         int32_t* status, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int64_t threads = n * 16;
+    int64_t blocks = (threads + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(c->num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (c->key_dtype == IDX_KEY_FP8_E4M3)
+        store_keys_kernel<true><<<static_cast<int>(blocks), 256, 0, st>>>(
+            static_cast<const uint4*>(k), slots, n, c->pool, c->num_blocks, c->block_size,
+            c->block_bytes, status);
+    else
+        store_keys_kernel<false><<<static_cast<int>(blocks), 256, 0, st>>>(
+            static_cast<const uint4*>(k), slots, n, c->pool, c->num_blocks, c->block_size,
+            c->block_bytes, status);
+    return cudaGetLastError();
+}
+
+}  // namespace dsaidx

@@ -1,0 +1,244 @@
+// topk.cuh -- block-level exact top-k machinery (256 threads per block).
+//
+// Every candidate is a 64-bit composite (score_key << 32) | ~index: the order
+// of composites is "higher score first, then lower index", the tie rule of the
+// library, and composites are unique within one query row.  Selection works on
+// a 4096-bin histogram of the top 12 bits of score_key followed by exact radix
+// refinement of the boundary bin, and finishes with a bitonic sort of the k
+// winners.
+#pragma once
+
+#include "common.cuh"
+
+namespace dsaidx {
+
+constexpr int kTopkThreads = 256;
+
+__device__ __forceinline__ uint64_t make_comp(uint32_t key, int32_t idx) {
+    return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(idx));
+}
+__device__ __forceinline__ int32_t comp_index(uint64_t c) {
+    return static_cast<int32_t>(~static_cast<uint32_t>(c & 0xFFFFFFFFull));
+}
+__device__ __forceinline__ uint32_t comp_key(uint64_t c) { return static_cast<uint32_t>(c >> 32); }
+__device__ __forceinline__ uint32_t key_bin(uint32_t key) { return key >> kHistShift; }
+
+// Warp-aggregated shared-memory histogram increment (one atomic per distinct
+// bin in the warp).  Every lane of the warp must call it; `valid` masks lanes.
+__device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, bool valid) {
+    unsigned active = __ballot_sync(0xffffffffu, valid);
+    if (valid) {
+        unsigned peers = __match_any_sync(active, bin);
+        if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(peers) - 1))
+            atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
+    }
+}
+
+struct Boundary {
+    int bin;          // largest bin whose suffix count reaches `need` (-1: total < need)
+    uint32_t above;   // candidates in bins strictly above `bin` (the total when bin = -1)
+    uint32_t at;      // candidates inside `bin` (0 when bin = -1)
+};
+
+// Find the bin holding the need-th largest candidate of a histogram of nbins
+// (a multiple of 256) bins.  Called by all 256 threads; scratch holds >= 256
+// words.  Result in *out (shared), valid after the call for every thread.
+__device__ __forceinline__ void block_find_suffix(const uint32_t* hist, int nbins, uint32_t need,
+                                  uint32_t* scratch, Boundary* out) {
+    const int tid = threadIdx.x;
+    const int per = nbins / kTopkThreads;
+    uint32_t s = 0;
+    for (int i = 0; i < per; ++i) s += hist[tid * per + i];
+    scratch[tid] = s;
+    __syncthreads();
+    if (tid < 32) {
+        // lane l owns partials [8l, 8l + 8)
+        uint32_t ls = 0;
+        for (int i = 0; i < 8; ++i) ls += scratch[tid * 8 + i];
+        uint32_t incl = ls;  // sum over lanes >= l
+        for (int o = 1; o < 32; o <<= 1) {
+            uint32_t v = __shfl_down_sync(0xffffffffu, incl, o);
+            if (tid + o < 32) incl += v;
+        }
+        uint32_t after = incl - ls;  // sum over lanes > l
+        uint32_t total = __shfl_sync(0xffffffffu, incl, 0);
+        if (total < need) {
+            if (tid == 0) {
+                out->bin = -1;
+                out->above = total;
+                out->at = 0;
+            }
+        } else if (after < need && need <= incl) {
+            uint32_t acc = after;
+            int p = tid * 8;
+            for (int j = 7; j >= 0; --j) {
+                uint32_t v = scratch[tid * 8 + j];
+                if (acc + v >= need) {
+                    p = tid * 8 + j;
+                    break;
+                }
+                acc += v;
+            }
+            for (int j = per - 1; j >= 0; --j) {
+                uint32_t v = hist[p * per + j];
+                if (acc + v >= need) {
+                    out->bin = p * per + j;
+                    out->above = acc;
+                    out->at = v;
+                    break;
+                }
+                acc += v;
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// Shared scratch of the selection routines.
+struct SelectSmem {
+    uint32_t hist256[256];
+    uint32_t scratch[256];
+    Boundary bnd;
+    uint32_t nsel;       // entries in sel
+    uint32_t nbnd;       // entries seen in the boundary bin
+    uint64_t thr;        // composite threshold of the boundary refinement
+};
+
+// Exact refinement inside one bin: among the candidate set X (all composites
+// whose top 12 bits equal `bin`), find the composite threshold thr such that
+// exactly m members of X are >= thr.  `each(f)` must call f(comp) for every
+// candidate of the full set, strided over the block's threads (it may visit
+// composites outside X; they are filtered here).  Called by all 256 threads.
+template <class Each>
+__device__ uint64_t radix_refine(Each each, int bin, uint32_t m, SelectSmem* ss) {
+    uint64_t prefix = static_cast<uint64_t>(bin) << 52;
+    uint64_t mask = 0xFFFull << 52;
+    uint32_t need = m;
+    const int shifts[7] = {44, 36, 28, 20, 12, 4, 0};
+    for (int pass = 0; pass < 7; ++pass) {
+        const int sh = shifts[pass];
+        const uint64_t dmask = (pass == 6) ? 0xFull : 0xFFull;
+        ss->hist256[threadIdx.x] = 0;
+        __syncthreads();
+        each([&](uint64_t c) {
+            if ((c & mask) == prefix) atomicAdd(&ss->hist256[(c >> sh) & dmask], 1u);
+        });
+        __syncthreads();
+        block_find_suffix(ss->hist256, 256, need, ss->scratch, &ss->bnd);
+        const int d = ss->bnd.bin;   // never -1: X holds at least `need` members
+        const uint32_t above = ss->bnd.above;
+        const uint32_t at = ss->bnd.at;
+        __syncthreads();
+        need -= above;
+        prefix |= static_cast<uint64_t>(d) << sh;
+        mask |= dmask << sh;
+        if (at == need) break;  // every member with this prefix is selected
+    }
+    return prefix;
+}
+
+// In-place bitonic sort, descending, of n (power of two, <= 4096) composites.
+__device__ __forceinline__ void bitonic_sort_desc(uint64_t* a, int n) {
+    for (int size = 2; size <= n; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < n / 2; i += kTopkThreads) {
+                int lo = 2 * i - (i & (stride - 1));
+                int hi = lo + stride;
+                bool desc = ((lo & size) == 0);
+                uint64_t x = a[lo], y = a[hi];
+                if ((x < y) == desc) {
+                    a[lo] = y;
+                    a[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__device__ __forceinline__ int next_pow2(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+// Final selection of one query row from a candidate set whose 4096-bin
+// histogram `hist` (shared) is exact.  `each(f)` visits every candidate
+// composite (strided over the block).  sel: shared buffer of >= next_pow2(k)
+// composites; bndbuf: shared buffer of bcap composites.  Writes the k outputs
+// (descending, -1 / -inf padded).  Called by all 256 threads.
+template <class Each>
+__device__ void select_topk_from_hist(Each each, const uint32_t* hist, int k, uint64_t* sel,
+                                      uint64_t* bndbuf, int bcap, SelectSmem* ss,
+                                      int32_t* out_idx, float* out_score) {
+    const int tid = threadIdx.x;
+    block_find_suffix(hist, kHistBins, static_cast<uint32_t>(k), ss->scratch, &ss->bnd);
+    const int bstar = ss->bnd.bin;
+    const uint32_t above = ss->bnd.above;
+    if (tid == 0) {
+        ss->nsel = 0;
+        ss->nbnd = 0;
+    }
+    __syncthreads();
+    // gather: bins above the boundary go straight to sel, the boundary bin to bndbuf
+    each([&](uint64_t c) {
+        int b = static_cast<int>(comp_key(c) >> kHistShift);
+        if (b > bstar) {
+            uint32_t p = atomicAdd(&ss->nsel, 1u);
+            sel[p] = c;
+        } else if (b == bstar) {
+            uint32_t p = atomicAdd(&ss->nbnd, 1u);
+            if (p < static_cast<uint32_t>(bcap)) bndbuf[p] = c;
+        }
+    });
+    __syncthreads();
+    if (bstar >= 0) {
+        const uint32_t m = static_cast<uint32_t>(k) - above;
+        const uint32_t nb = ss->nbnd;
+        if (nb == m) {
+            for (uint32_t i = tid; i < nb; i += kTopkThreads) sel[above + i] = bndbuf[i];
+        } else {
+            uint64_t thr;
+            if (nb <= static_cast<uint32_t>(bcap)) {
+                thr = radix_refine(
+                    [&](auto f) {
+                        for (uint32_t i = tid; i < nb; i += kTopkThreads) f(bndbuf[i]);
+                    },
+                    bstar, m, ss);
+            } else {
+                thr = radix_refine(each, bstar, m, ss);
+            }
+            if (tid == 0) ss->nsel = above;
+            __syncthreads();
+            if (nb <= static_cast<uint32_t>(bcap)) {
+                for (uint32_t i = tid; i < nb; i += kTopkThreads) {
+                    uint64_t c = bndbuf[i];
+                    if (c >= thr) sel[atomicAdd(&ss->nsel, 1u)] = c;
+                }
+            } else {
+                each([&](uint64_t c) {
+                    if (static_cast<int>(comp_key(c) >> kHistShift) == bstar && c >= thr)
+                        sel[atomicAdd(&ss->nsel, 1u)] = c;
+                });
+            }
+        }
+        __syncthreads();
+    }
+    const int nsel = (bstar >= 0) ? k : static_cast<int>(above);
+    const int n2 = next_pow2(nsel < 1 ? 1 : nsel);
+    for (int i = nsel + tid; i < n2; i += kTopkThreads) sel[i] = 0ull;
+    __syncthreads();
+    bitonic_sort_desc(sel, n2);
+    for (int j = tid; j < k; j += kTopkThreads) {
+        if (j < nsel) {
+            uint64_t c = sel[j];
+            out_idx[j] = comp_index(c);
+            if (out_score) out_score[j] = key_score(comp_key(c));
+        } else {
+            out_idx[j] = -1;
+            if (out_score) out_score[j] = -INFINITY;
+        }
+    }
+}
+
+}  // namespace dsaidx

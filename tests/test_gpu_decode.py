@@ -1,0 +1,136 @@
+"""GPU parity of idx_score_topk_decode (fused score + top-k, one query per
+sequence) against the CPU oracle, on the decode workloads at full size and on
+ragged / degenerate cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_attention_top_idx_gb300 import dsaidx
+from sparse_attention_top_idx_gb300 import workloads as wl
+from tests.parity import build_cache, check_rows, decode_inputs, run_decode
+
+pytestmark = pytest.mark.gpu
+
+
+def oracle_ref(W, mode, rows=None):
+    rows = list(range(W.batch)) if rows is None else rows
+    keys = [oracle.quantize_rows(W.keys[b]) if mode == oracle.FP8 else W.keys[b] for b in rows]
+    q = W.q[rows]
+    w = W.w[rows]
+    pos = np.asarray([W.seq_lens[b] - 1 for b in rows], np.int64)
+    ref = oracle.score_topk(mode, W.topk, q, w, np.arange(len(rows), dtype=np.int32), pos, keys,
+                            full_scores=True)
+    return ref, pos + 1
+
+
+def check(W, mode, got, rows=None):
+    rows = list(range(W.batch)) if rows is None else rows
+    ref, nvis = oracle_ref(W, mode, rows)
+    return check_rows(got, ref, nvis, W.topk, rows=rows)
+
+
+@pytest.mark.parametrize("bs", [32, 64])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_ragged_small(bs, mode):
+    # lengths around tile / block / k boundaries, k larger than some sequences
+    W = wl.make_workload("ragged", [700, 129, 1, 128, 64, 2049, 513, 0], [1] * 8, topk=128, bs=bs,
+                         seed=31 + bs + mode)
+    got = run_decode(W, mode)
+    check(W, mode, got)
+    assert np.all(got["idx"][7] == -1)           # empty sequence
+
+
+@pytest.mark.parametrize("k", [512, 1024])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_precision_workload(mode, k):
+    # 4 sequences of 2000 / 4500 / 10000 / 22000 keys with a planted needle
+    W = wl.precision_compare(topk=k)
+    got = run_decode(W, mode)
+    check(W, mode, got)
+    for b in range(W.batch):
+        assert got["idx"][b][0] == W.needle_pos[b]      # the needle ranks first
+
+
+def test_decode_batch_full_size():
+    # 32 sequences alternating 4500 / 10000 keys, top-512, fp8, blocks of 64
+    W = wl.decode_batch()
+    got = run_decode(W, dsaidx.FP8)
+    exact = check(W, dsaidx.FP8, got)
+    assert exact >= 30
+    for b in range(W.batch):
+        assert got["idx"][b][0] == W.needle_pos[b]
+
+
+def test_long_context_full_size_sampled():
+    # 8 x 131072 + 1 x 1048576 keys, top-1024: the GPU runs the whole batch;
+    # the oracle checks one 131072-key row and the 1M-key row
+    W = wl.long_context()
+    got = run_decode(W, dsaidx.FP8)
+    check(W, dsaidx.FP8, got, rows=[3, 8])
+    for b in range(W.batch):
+        idx = got["idx"][b]
+        assert len(np.unique(idx)) == 1024 and idx.min() >= 0 and idx.max() < W.seq_lens[b]
+        assert idx[0] == W.needle_pos[b]
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_ties_go_to_lower_index(mode):
+    # every key identical: all scores tie, so the top-k is the first k positions
+    W = wl.make_workload("ties", [3000, 300], [1, 1], topk=256, seed=4)
+    for b in range(W.batch):
+        W.keys[b][:] = W.keys[b][0]
+    got = run_decode(W, mode)
+    assert np.array_equal(got["idx"][0], np.arange(256))
+    assert np.array_equal(got["idx"][1], np.arange(256))
+    assert np.all(got["score"][0] == got["score"][0][0])
+    # more tied candidates than the selection keeps in shared memory
+    W3 = wl.make_workload("ties3", [10000], [1], topk=100, seed=6)
+    W3.keys[0][:] = W3.keys[0][0]
+    got3 = run_decode(W3, mode)
+    assert np.array_equal(got3["idx"][0], np.arange(100))
+    # groups of duplicates: many exact ties at the boundary
+    W2 = wl.make_workload("ties2", [5000], [1], topk=300, seed=5)
+    W2.keys[0][:] = W2.keys[0][np.arange(5000) % 37]
+    got2 = run_decode(W2, mode)
+    check(W2, mode, got2)
+
+
+def test_deterministic_and_workspace_reuse():
+    W = wl.make_workload("det", [4500, 10000, 300, 7777], [1] * 4, topk=512, seed=8)
+    outs = run_decode(W, dsaidx.FP8, reps=5)
+    for o in outs[1:]:
+        assert np.array_equal(o["idx"], outs[0]["idx"])
+        assert np.array_equal(o["score"].view(np.uint32), outs[0]["score"].view(np.uint32))
+    check(W, dsaidx.FP8, outs[-1])
+
+
+def test_bad_block_id_flags_row():
+    W = wl.make_workload("bad", [1000, 1000], [1, 1], topk=64, seed=9)
+    cache = build_cache(W, dsaidx.FP8)
+    W.block_table[1, 3] = W.num_blocks + 5       # outside the pool
+    got = run_decode(W, dsaidx.FP8, cache=cache, expect_status=5)
+    assert np.all(got["idx"][1] == -1)
+    ref, nvis = oracle_ref(W, dsaidx.FP8, [0])
+    check_rows(got, ref, nvis, 64, rows=[0])
+
+
+def test_seq_len_above_bound_flags_row():
+    W = wl.make_workload("over", [1000, 600], [1, 1], topk=64, seed=10)
+    got = run_decode(W, dsaidx.FP8, max_seq_len=800, expect_status=5)
+    assert np.all(got["idx"][0] == -1)
+    ref, nvis = oracle_ref(W, dsaidx.FP8, [1])
+    check_rows(got, ref, nvis, 64, rows=[1])
+
+
+def test_workspace_too_small_is_rejected():
+    W = wl.make_workload("ws", [300], [1], topk=64, seed=11)
+    cache = build_cache(W, dsaidx.FP8)
+    ins = decode_inputs(W)
+    need = dsaidx.workspace_bytes_decode(cache, 1, 300, 64, 64)
+    ws = dsaidx.new_workspace(need - 256)
+    oi = torch.empty((1, 64), dtype=torch.int32, device="cuda")
+    with pytest.raises(dsaidx.IdxError) as e:
+        dsaidx.score_topk_decode(cache, ins["q"], ins["w"], ins["block_table"], ins["seq_lens"], 300, 64,
+                                 oi, ws)
+    assert e.value.code == 4

@@ -1,0 +1,91 @@
+"""GPU parity of idx_score_topk_prefill (causal query chunks) against the CPU
+oracle: the tiny workload in full, ragged multi-sequence chunks, the long
+prefill chunk at full size (sampled rows against the oracle, every row against
+the selection invariants), and decode / prefill agreement."""
+import numpy as np
+import pytest
+
+import oracle
+from sparse_attention_top_idx_gb300 import dsaidx
+from sparse_attention_top_idx_gb300 import workloads as wl
+from tests.parity import build_cache, check_rows, run_decode, run_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+def oracle_ref(W, mode, rows=None):
+    R = W.total_q
+    rows = list(range(R)) if rows is None else list(rows)
+    keys = [oracle.quantize_rows(k) if mode == oracle.FP8 else k for k in W.keys]
+    ref = oracle.score_topk(mode, W.topk, W.q[rows], W.w[rows], W.row_seq()[rows], W.row_pos()[rows],
+                            keys, full_scores=True)
+    return ref, W.row_pos()[rows] + 1
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_tiny_prefill(mode):
+    # 1 sequence of 2000 keys, queries at its last 16 positions, top-512
+    W = wl.tiny_prefill()
+    got = run_prefill(W, mode)
+    ref, nvis = oracle_ref(W, mode)
+    exact = check_rows(got, ref, nvis, W.topk)
+    assert exact >= 14
+    for r in range(W.total_q):
+        assert got["idx"][r][0] == W.needle_pos[0]
+
+
+@pytest.mark.parametrize("bs", [32, 64])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_ragged_chunks(bs, mode):
+    # several sequences, chunk sizes not multiples of 4 queries, rows that see
+    # fewer keys than k, a one-query chunk
+    W = wl.make_workload("rag", [300, 1000, 129, 70], [7, 130, 1, 70], topk=128, bs=bs,
+                         seed=40 + bs + mode)
+    got = run_prefill(W, mode)
+    ref, nvis = oracle_ref(W, mode)
+    check_rows(got, ref, nvis, W.topk)
+
+
+def test_prefill_chunk_full_size_sampled():
+    # 1 sequence of 22000 keys, queries at its last 8192 positions, top-1024
+    W = wl.prefill_chunk()
+    got = run_prefill(W, dsaidx.FP8)
+    T = W.total_q
+    rows = sorted(set([0, 1, 2, 3, 4, 5, 127, 128, 129, 4095, 4096, T - 5, T - 4, T - 3, T - 2, T - 1]
+                      + list(range(7, T, 613))))
+    ref, nvis = oracle_ref(W, dsaidx.FP8, rows)
+    check_rows(got, ref, nvis, W.topk, rows=rows)
+    pos = W.row_pos()
+    idx = got["idx"]
+    assert np.all(idx >= 0)
+    assert np.all(idx.max(axis=1) <= pos)
+    s = np.sort(idx, axis=1)
+    assert np.all(np.diff(s, axis=1) > 0)                 # no duplicates in any row
+    assert np.all(np.diff(got["score"], axis=1) <= 0)     # descending in every row
+    assert np.all(idx[:, 0] == W.needle_pos[0])
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_last_prefill_row_equals_decode(mode):
+    # decode is the one-query chunk: same scores and selection for the last row
+    W = wl.make_workload("x", [3000, 1500], [9, 4], topk=256, seed=12)
+    cache = build_cache(W, mode)
+    pre = run_prefill(W, mode, cache=cache)
+    cu = W.cu_seqlens_q()
+    D = wl.Workload("x1", W.seq_lens, [1, 1], W.H, W.d, W.topk, W.bs, W.keys,
+                    W.q[cu[1:] - 1], W.w[cu[1:] - 1], W.needle_pos, W.block_table, W.num_blocks)
+    dec = run_decode(D, mode, cache=cache)
+    for b in range(2):
+        r = cu[b + 1] - 1
+        assert np.array_equal(pre["idx"][r], dec["idx"][b])
+        assert np.array_equal(pre["score"][r].view(np.uint32), dec["score"][b].view(np.uint32))
+
+
+def test_bad_block_id_flags_rows():
+    W = wl.make_workload("bad", [500, 400], [5, 6], topk=64, seed=13)
+    cache = build_cache(W, dsaidx.FP8)
+    W.block_table[0, 2] = -3
+    got = run_prefill(W, dsaidx.FP8, cache=cache, expect_status=5)
+    assert np.all(got["idx"][:5] == -1)
+    ref, nvis = oracle_ref(W, dsaidx.FP8, range(5, 11))
+    check_rows(got, ref, nvis, 64, rows=range(5, 11))

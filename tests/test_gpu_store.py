@@ -1,0 +1,87 @@
+"""GPU parity of idx_store_keys against the oracle's store: every byte of the
+pool (codes, scales, untouched canary bytes) must match bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_attention_top_idx_gb300 import dsaidx
+from sparse_attention_top_idx_gb300 import workloads as wl
+from tests.parity import bf16_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+def oracle_pool(W, mode, k_bits, slots, fill=0xA5):
+    bb = oracle.block_bytes(mode, W.bs)
+    pool = np.full(W.num_blocks * bb, fill, np.uint8)
+    oracle.store_keys(pool, k_bits, slots, W.bs, mode)
+    return pool
+
+
+@pytest.mark.parametrize("bs", [32, 64])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_store_bit_exact(bs, mode):
+    W = wl.make_workload("st", [1000, 77, 64, 3000], [1, 1, 1, 1], bs=bs, seed=10 + bs + mode,
+                         extra_blocks=5)
+    k = W.all_keys().copy()
+    slots = W.all_slots().copy()
+    # some tokens skipped with a negative slot
+    slots[::17] = -1
+    # keys over a wide range of magnitudes, including tiny rows that hit the
+    # e4m3 subnormals and an all-zero row
+    rng = np.random.default_rng(bs + mode)
+    scale = (10.0 ** rng.uniform(-30, 30, (k.shape[0], 1))).astype(np.float32)
+    kf = wl.bf16_bits_to_f32(k) * scale
+    kf[5] = 0.0
+    k = wl.f32_to_bf16_bits(kf)
+    cache = dsaidx.IndexCache.allocate(W.num_blocks, bs, mode, fill=0xA5)
+    dsaidx.store_keys(cache, bf16_tensor(k), torch.from_numpy(slots).cuda())
+    got = cache.pool.cpu().numpy()
+    want = oracle_pool(W, mode, k, slots)
+    diff = np.nonzero(got != want)[0]
+    assert diff.size == 0, "first differing byte %d of %d" % (diff[0], diff.size)
+
+
+def test_e4m3_convert_every_bf16_below_448():
+    # Rows whose largest magnitude is 448 have scale exactly 1, so the codes
+    # are the e4m3 encodings of the bf16 values themselves: every finite bf16
+    # magnitude up to 448, both signs, against the oracle's encoder.
+    pos = np.arange(0, 0x43E1, dtype=np.uint16)          # bf16 0 .. 448
+    vals = np.concatenate([pos, pos | 0x8000])
+    per = 127
+    nrows = (len(vals) + per - 1) // per
+    rows = np.zeros((nrows, 128), np.uint16)
+    rows[:, 0] = 0x43E0                                    # 448.0
+    flat = np.zeros(nrows * per, np.uint16)
+    flat[:len(vals)] = vals
+    rows[:, 1:] = flat.reshape(nrows, per)
+    bs = 64
+    nblk = (nrows + bs - 1) // bs
+    cache = dsaidx.IndexCache.allocate(nblk, bs, dsaidx.FP8, fill=0)
+    slots = np.arange(nrows, dtype=np.int64)
+    dsaidx.store_keys(cache, bf16_tensor(rows), torch.from_numpy(slots).cuda())
+    got = cache.pool.cpu().numpy().reshape(nblk, 8448)
+    codes = np.concatenate([got[b, :bs * 128].reshape(bs, 128) for b in range(nblk)])[:nrows]
+    scales = np.concatenate([got[b, bs * 128:].view(np.float32) for b in range(nblk)])[:nrows]
+    assert np.all(scales == 1.0)
+    want, _ = oracle.quantize_rows(rows)
+    assert np.array_equal(codes, want)
+
+
+def test_out_of_range_slot_sets_status_and_skips():
+    bs = 64
+    cache = dsaidx.IndexCache.allocate(2, bs, dsaidx.FP8, fill=0x11)
+    k = bf16_tensor(wl.f32_to_bf16_bits(np.ones((3, 128), np.float32)))
+    slots = torch.tensor([0, 2 * bs, 5], dtype=torch.int64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dsaidx.store_keys(cache, k, slots, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5
+    pool = cache.pool.cpu().numpy()
+    assert np.all(pool[:128] == 0x7E) and np.all(pool[5 * 128:6 * 128] == 0x7E)
+    # nothing else written
+    mask = np.ones(pool.size, bool)
+    mask[:128] = mask[5 * 128:6 * 128] = False
+    mask[8192:8196] = mask[8192 + 20:8192 + 24] = False
+    assert np.all(pool[mask] == 0x11)
