@@ -1,0 +1,472 @@
+"""Benchmark of the DSA indexer hot path on GB300.
+
+One step = one decode step of the 32-sequence batch (context lengths
+alternating 4500 / 10000, 1 query each, 64 index heads x 128 dims, top-512,
+fp8 e4m3 paged keys in blocks of 64): idx_store_keys of the step's 32 new keys
+followed by idx_score_topk_decode over every cached key.  The metric is keys
+scored and selected per second (232,000 keys per step); microseconds per step
+are reported beside it.  Inputs are seeded synthetic data resident in HBM; 9
+copies of the paged pool (275 MB, more than twice the L2) are rotated so that
+every step reads its keys from HBM.
+
+Also reported, as nested objects of the same JSON line: the long-context decode
+batch (8 x 131072 + 1 x 1048576 keys, top-1024) and the 8192-query causal
+prefill chunk over 22000 keys (top-1024), each with its own roofline.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 launch with torch.distributed.run; every rank runs an independent
+replica on its own GPU (the indexer has no exchange step on one node).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "indexer keys scored+selected/s (decode, 32 seqs x 4500/10000 keys, top-512, fp8)"
+UNIT = "keys/s"
+KEY_BYTES_FP8 = 132          # one fp8 index-key record: 128 e4m3 codes + fp32 scale
+N_POOL_COPIES = 9
+
+# DRAM bytes per launch of the dominant kernels from ncu captures
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
+# hash of the kernel sources they were taken on; a stale hash reports null.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "sparse_attention_top_idx_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the GPU is under load."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def setup_dist(n_gpus: int):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        dist.init_process_group(backend=backend)
+    return rank, world, local, dist
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+# decode workload
+# ----------------------------------------------------------------------------
+
+class DecodeBench:
+    def __init__(self, W, device, copies: int):
+        import torch
+        from sparse_attention_top_idx_gb300 import dsaidx
+        from tests.parity import bf16_tensor
+        self.W = W
+        self.device = device
+        self.dsaidx = dsaidx
+        B, k = W.batch, W.topk
+        k_all = bf16_tensor(W.all_keys(), device)
+        slots_all = torch.from_numpy(W.all_slots()).to(device)
+        self.caches = []
+        for _ in range(copies):
+            c = dsaidx.IndexCache.allocate(W.num_blocks, W.bs, dsaidx.FP8, device=device, fill=0)
+            dsaidx.store_keys(c, k_all, slots_all)
+            self.caches.append(c)
+        del k_all
+        # the step's new keys: the last position of every sequence
+        last = np.concatenate([np.cumsum(W.seq_lens) - 1])
+        self.new_k = bf16_tensor(W.all_keys()[last], device)
+        self.new_slots = slots_all[torch.from_numpy(last).to(device)].contiguous()
+        self.q = bf16_tensor(W.q, device)
+        self.w = torch.from_numpy(W.w).to(device)
+        self.bt = torch.from_numpy(W.block_table).to(device)
+        self.sl = torch.tensor(W.seq_lens, dtype=torch.int32, device=device)
+        self.msl = W.max_seq_len
+        self.ws = dsaidx.new_workspace(dsaidx.workspace_bytes_decode(self.caches[0], B, self.msl, W.H, k),
+                                       device)
+        self.out = torch.empty((B, k), dtype=torch.int32, device=device)
+        self.keys = int(sum(W.seq_lens))
+
+    def step(self, i, ev=None):
+        c = self.caches[i % len(self.caches)]
+        self.dsaidx.store_keys(c, self.new_k, self.new_slots)
+        if ev is not None:
+            ev[0].record()
+        self.dsaidx.score_topk_decode(c, self.q, self.w, self.bt, self.sl, self.msl, self.W.topk, self.out,
+                                      self.ws)
+        if ev is not None:
+            ev[1].record()
+
+    def algo_bytes(self):
+        W = self.W
+        return (self.keys * KEY_BYTES_FP8 + W.q.nbytes + W.w.nbytes + W.batch * W.topk * 4
+                + W.block_table.nbytes)
+
+
+def time_steps(bench, steps, warmup, dist, device):
+    """W warm-up steps, then exactly K timed steps between barriers and
+    synchronisations; per-step events around the scoring kernel."""
+    import torch
+    for i in range(warmup):
+        bench.step(i)
+    torch.cuda.synchronize(device)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    t0.record()
+    for i in range(steps):
+        bench.step(warmup + i, evs[i])
+    t1.record()
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    total_ms = t0.elapsed_time(t1)
+    kern_ms = [a.elapsed_time(b) for a, b in evs]
+    return total_ms, kern_ms
+
+
+def load_padding(bench, seconds, device):
+    """Keep the GPU busy (untimed) so the clock sampler sees the same load."""
+    import torch
+    t_end = time.time() + seconds
+    i = 0
+    while time.time() < t_end:
+        for _ in range(50):
+            bench.step(i)
+            i += 1
+        torch.cuda.synchronize(device)
+
+
+def e2e_decode(bench, steps, warmup, device):
+    """Same decode step through the public API from pinned host buffers: every
+    step copies the step's inputs host->device (queries, head weights, sequence
+    lengths, the new keys and their slots) and reads the selected indices back."""
+    import torch
+    W = bench.W
+    h_q = bench.q.cpu().pin_memory()
+    h_w = bench.w.cpu().pin_memory()
+    h_sl = bench.sl.cpu().pin_memory()
+    h_k = bench.new_k.cpu().pin_memory()
+    h_s = bench.new_slots.cpu().pin_memory()
+    h_out = torch.empty_like(bench.out, device="cpu").pin_memory()
+    d_q, d_w, d_sl = torch.empty_like(bench.q), torch.empty_like(bench.w), torch.empty_like(bench.sl)
+    d_k, d_s = torch.empty_like(bench.new_k), torch.empty_like(bench.new_slots)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_w, h_sl, h_k, h_s))
+    d2h = h_out.numel() * h_out.element_size()
+    ds = bench.dsaidx
+
+    def one(i):
+        c = bench.caches[i % len(bench.caches)]
+        d_q.copy_(h_q, non_blocking=True)
+        d_w.copy_(h_w, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_s.copy_(h_s, non_blocking=True)
+        ds.store_keys(c, d_k, d_s)
+        ds.score_topk_decode(c, d_q, d_w, bench.bt, d_sl, bench.msl, W.topk, bench.out, bench.ws)
+        h_out.copy_(bench.out, non_blocking=True)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize(device)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(steps):
+        one(warmup + i)
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / steps
+    return ms, h2d, d2h
+
+
+def roofline_hbm(algo_bytes, kern_ms, peak_gbs, traffic):
+    avg_ms = float(np.mean(kern_ms))
+    ach = algo_bytes / (avg_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak_gbs, "unit": "GB/s",
+            "frac": round(ach / peak_gbs, 4), "traffic": traffic,
+            "kernel_us": round(avg_ms * 1e3, 3), "algorithmic_bytes": int(algo_bytes)}
+
+
+def bench_long_context(device, steps, warmup, peaks, src_hash):
+    import torch
+    from sparse_attention_top_idx_gb300 import workloads as wl
+    W = wl.long_context()
+    b = DecodeBench(W, device, copies=2)     # 277 MB per copy: larger than L2
+    total_ms, kern_ms = time_steps(b, steps, warmup, None, device)
+    tr = NCU_TRAFFIC.get(("longctx", src_hash))
+    out = {"workload": W.name, "keys_per_step": b.keys, "ms_per_step": round(total_ms / steps, 5),
+           "value": round(b.keys / (total_ms / steps * 1e-3), 1), "unit": UNIT,
+           "roofline": roofline_hbm(b.algo_bytes(), kern_ms, peaks["hbm_gbs"], tr)}
+    del b
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_prefill(device, steps, warmup, peaks, src_hash):
+    import torch
+    from sparse_attention_top_idx_gb300 import dsaidx
+    from sparse_attention_top_idx_gb300 import workloads as wl
+    from tests.parity import bf16_tensor, build_cache
+    W = wl.prefill_chunk()
+    cache = build_cache(W, dsaidx.FP8, device=device)
+    T, k = W.total_q, W.topk
+    q = bf16_tensor(W.q, device)
+    w = torch.from_numpy(W.w).to(device)
+    cu = torch.from_numpy(W.cu_seqlens_q()).to(device)
+    sl = torch.tensor(W.seq_lens, dtype=torch.int32, device=device)
+    bt = torch.from_numpy(W.block_table).to(device)
+    ws = dsaidx.new_workspace(dsaidx.workspace_bytes_prefill(cache, 1, T, W.max_seq_len, W.H, k), device)
+    oi = torch.empty((T, k), dtype=torch.int32, device=device)
+    for _ in range(warmup):
+        dsaidx.score_topk_prefill(cache, q, w, cu, sl, bt, W.max_seq_len, k, oi, ws)
+    torch.cuda.synchronize(device)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        dsaidx.score_topk_prefill(cache, q, w, cu, sl, bt, W.max_seq_len, k, oi, ws)
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / steps
+    pairs = int(np.sum(W.row_pos() + 1))
+    flops = 2.0 * pairs * W.H * W.d
+    fp8_peak = peaks["bf16_tflops"] * 2.0          # nominal fp8 : bf16 dense ratio 2
+    ach = flops / (ms * 1e-3) / 1e12
+    out = {"workload": W.name, "pairs_per_step": pairs, "ms_per_step": round(ms, 4),
+           "value": round(pairs / (ms * 1e-3), 1), "unit": "query-key pairs/s",
+           "roofline": {"bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_peak, 1),
+                        "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4),
+                        "traffic": NCU_TRAFFIC.get(("prefill", src_hash)),
+                        "note": "whole call (score kernel + row select); fp8 peak = measured bf16 x 2"}}
+    del cache, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# ----------------------------------------------------------------------------
+
+def oracle_decode_rate(W, budget_s: float):
+    """Time the oracle on whole decode steps of the workload (keys already
+    quantised, as they sit in the cache) until about budget_s has passed."""
+    import oracle
+    keys = [oracle.quantize_rows(k) for k in W.keys]
+    pos = np.asarray(W.seq_lens, np.int64) - 1
+    rows = np.arange(W.batch, dtype=np.int32)
+    last = np.cumsum(W.seq_lens) - 1
+    newk = W.all_keys()[last]
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.quantize_rows(newk)                  # the step's new keys
+        oracle.score_topk(oracle.FP8, W.topk, W.q, W.w, rows, pos, keys)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    keys_total = reps * int(sum(W.seq_lens))
+    return keys_total / el, oracle.num_threads(), reps, el
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from sparse_attention_top_idx_gb300 import workloads as wl
+    W = wl.decode_batch()
+    budget = max(2.0, min(60.0, 1.5 * (args.steps + args.warmup)))
+    rate, cores, reps, el = oracle_decode_rate(W, budget)
+    line = {"impl": "reference", "metric": METRIC, "value": round(rate, 1), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": reps, "warmup": 0,
+            "ms_per_step": round(1e3 * el / reps, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulation)", "data": "synthetic",
+            "config": config_dict(W),
+            "cpu_baseline": {"value": round(rate, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "%d whole decode steps (32 rows, all keys) in %.1f s" % (reps, el)},
+            "e2e": {"value": round(rate, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def config_dict(W):
+    return {"workload": W.name, "batch": W.batch, "seq_lens": "4500/10000 alternating",
+            "keys_per_step": int(sum(W.seq_lens)), "heads": W.H, "head_dim": W.d, "topk": W.topk,
+            "block_size": W.bs, "key_format": "fp8 e4m3 + fp32 scale (132 B/token)",
+            "step": "idx_store_keys(32 new keys) + idx_score_topk_decode",
+            "l2": "rotating %d pool copies (%.0f MB) so each step reads its keys from HBM"
+                  % (N_POOL_COPIES, N_POOL_COPIES * sum(W.seq_lens) * KEY_BYTES_FP8 / 1e6)}
+
+
+# ----------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the long-context and prefill objects")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import __graft_entry__
+    rank, world, local, dist = setup_dist(args.gpus)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0:
+        __graft_entry__.build()
+    barrier(dist)
+    from sparse_attention_top_idx_gb300 import dsaidx, workloads as wl
+    dsaidx.load()
+    peaks = measured_peaks()
+    src_hash = kernel_source_hash()
+
+    W = wl.decode_batch()
+    bench = DecodeBench(W, device, N_POOL_COPIES)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    total_ms, kern_ms = time_steps(bench, args.steps, args.warmup, dist, device)
+    load_padding(bench, 1.0, device)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(total_ms, dist, device)
+    ms_step = total_ms / args.steps
+    value = world * bench.keys / (ms_step * 1e-3)
+
+    e2e_ms, h2d, d2h = e2e_decode(bench, args.steps, args.warmup, device)
+    e2e_ms = max_over_ranks(e2e_ms, dist, device)
+
+    tr = NCU_TRAFFIC.get(("decode", src_hash))
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "us_per_step": round(ms_step * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulation)",
+            "data": "synthetic (seeded iid N(0,1) keys, planted needle)",
+            "config": config_dict(W),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "roofline": roofline_hbm(bench.algo_bytes(), kern_ms, peaks["hbm_gbs"], tr),
+            "peaks_source": peaks["source"],
+            "e2e": {"value": round(world * bench.keys / (e2e_ms * 1e-3), 1), "unit": UNIT,
+                    "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks}
+    del bench
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_extra:
+        line["long_context"] = bench_long_context(device, max(10, args.steps // 4), args.warmup, peaks, src_hash)
+        line["prefill"] = bench_prefill(device, max(3, args.steps // 40), 3, peaks, src_hash)
+    if rank == 0 and not args.no_cpu:
+        rate, cores, reps, el = oracle_decode_rate(W, 10.0)
+        line["cpu_baseline"] = {"value": round(rate, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": "%d whole decode steps (32 rows, all 232,000 keys) in %.1f s"
+                                          % (reps, el)}
+    if rank == 0:
+        print(json.dumps(line))
+    barrier(dist)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -46,7 +46,8 @@ bool same_device(const idx_cache* c) {
 
 // Decode workspace layout.
 struct DecodeWs {
-    size_t ctr, ghist, seqflag, cnt, cand, total;
+    size_t ctr, ghist, seqflag, seqcnt, cand, total;
+    int64_t cand_cap;
     int chunk, max_chunks;
 };
 DecodeWs decode_ws(const idx_cache* c, int batch, int max_seq_len) {
@@ -59,7 +60,8 @@ DecodeWs decode_ws(const idx_cache* c, int batch, int max_seq_len) {
     w.ctr = o;      o = align_up(o + nb * 4, 256);
     w.ghist = o;    o = align_up(o + nb * dsaidx::kHistBins * 4, 256);
     w.seqflag = o;  o = align_up(o + nb * 4, 256);
-    w.cnt = o;      o = align_up(o + units * 4, 256);
+    w.seqcnt = o;   o = align_up(o + nb * 4, 256);
+    w.cand_cap = static_cast<int64_t>(w.max_chunks) * w.chunk;
     w.cand = o;     o = align_up(o + units * static_cast<size_t>(w.chunk) * 8, 256);
     w.total = o;
     return w;
@@ -201,8 +203,9 @@ idx_status idx_score_topk_decode(const idx_cache* cache, const void* q_bf16_dev,
     p.ctr = reinterpret_cast<uint32_t*>(base + ws.ctr);
     p.ghist = reinterpret_cast<uint32_t*>(base + ws.ghist);
     p.seqflag = reinterpret_cast<uint32_t*>(base + ws.seqflag);
-    p.cnt = reinterpret_cast<uint32_t*>(base + ws.cnt);
+    p.seqcnt = reinterpret_cast<uint32_t*>(base + ws.seqcnt);
     p.cand = reinterpret_cast<uint64_t*>(base + ws.cand);
+    p.cand_cap = ws.cand_cap;
     cudaError_t e = dsaidx::launch_decode(cache, p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }

@@ -51,8 +51,9 @@ struct ScoreParams {
     uint32_t* ctr;               // decode: [batch] completed-chunk tickets
     uint32_t* ghist;             // decode: [batch, 4096] histogram of published candidates
     uint32_t* seqflag;           // decode: [batch] device-check flags
-    uint32_t* cnt;               // decode: [batch * max_chunks] candidates per chunk
-    uint64_t* cand;              // decode: [batch * max_chunks * chunk] composites
+    uint32_t* seqcnt;            // decode: [batch] candidates published per sequence
+    uint64_t* cand;              // decode: [batch, cand_cap] composites
+    int64_t cand_cap;            // decode: max_chunks * chunk (>= every seq_len)
     float* scores;               // prefill: [total_q, score_stride]
     int64_t score_stride;
     uint32_t* rowflag;           // prefill: [total_q]

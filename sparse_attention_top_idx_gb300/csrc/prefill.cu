@@ -65,16 +65,9 @@ __global__ void __launch_bounds__(kTopkThreads) prefill_select_kernel(const Scor
     }
     const int nvis = s_nvis;
     const float* row = p.scores + static_cast<int64_t>(r) * p.score_stride;
-    const int nround = (nvis + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
-    for (int i = tid; i < nround; i += kTopkThreads) {
-        const bool valid = i < nvis;
-        const uint32_t kk = valid ? score_key(__ldcg(row + i)) : 0u;
-        hist_add_warp(hist, key_bin(kk), valid);
-    }
+    auto each = [&](auto f) { walk_row(row, nvis, f); };
+    each([&](uint64_t c, bool v) { hist_add_warp(hist, key_bin(comp_key(c)), v); });
     __syncthreads();
-    auto each = [&](auto f) {
-        for (int i = tid; i < nvis; i += kTopkThreads) f(make_comp(score_key(__ldcg(row + i)), i));
-    };
     select_topk_from_hist(each, hist, p.topk, sel, bndbuf, kSelBcap, ss, oi, os);
 }
 

@@ -60,14 +60,27 @@ __device__ __forceinline__ int sw128_off(int r, int c) {
 // tile, and fill w'.  Row n = j * 64 + h (query j of the CTA, head h); rows of
 // missing queries (j >= nrows) get zero codes and zero weight.  fp8: per row
 // scale sq = amax / 448 (IEEE), codes e4m3(q / sq), w' = w * sq; amax = 0 gives
-// zero codes and w' = 0 * w.  Four threads per row, 32 elements each.
+// zero codes and w' = 0 * w.  Four consecutive threads per row (32 elements
+// each); t / nthreads: this thread's index among the nthreads doing the work.
+// Copy a 4096-bin histogram from global memory (bypassing L1) into shared
+// memory: four independent 16-byte loads per thread of a 256-thread block.
+__device__ __forceinline__ void copy_hist_global(uint32_t* dst, const uint32_t* src) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldcg(s4 + u * 256 + threadIdx.x);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) d4[u * 256 + threadIdx.x] = v[u];
+}
+
 template <bool kFp8, int kQT>
 __device__ __forceinline__ void prep_queries(const uint16_t* __restrict__ q, const float* __restrict__ w,
-                             int row0, int nrows, uint8_t* qtile, float* wq) {
+                             int row0, int nrows, uint8_t* qtile, float* wq, int t, int nthreads) {
     constexpr int kRows = 64 * kQT;
-    const int tid = threadIdx.x;
-    const int part = tid & 3;
-    for (int r = tid >> 2; r < kRows; r += kThreads / 4) {
+    const int part = t & 3;
+    const unsigned gmask = 0xFu << (threadIdx.x & 28);   // the 4 lanes sharing a row
+    for (int r = t >> 2; r < kRows; r += nthreads / 4) {
         const int j = r >> 6, h = r & 63;
         const bool have = j < nrows;
         uint4 v[4];
@@ -102,8 +115,8 @@ __device__ __forceinline__ void prep_queries(const uint16_t* __restrict__ q, con
             float amax = 0.0f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
             const float sq = __fdiv_rn(amax, 448.0f);
             uint32_t c[8];
 #pragma unroll
@@ -286,12 +299,17 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
     if constexpr (kDecode) {
         for (int i = tid; i < kHistBins; i += kThreads) hist[i] = 0;
     }
-    prep_queries<kFp8, kQT>(p.q, p.w, ks->row0, ks->nrows, qtile, wq);
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ks->tmem_base;
+    // Warp 0 starts streaming keys at once; warps 1..7 build the query tile
+    // meanwhile and meet on a named barrier before the first MMA.
+    if (warp != 0) {
+        prep_queries<kFp8, kQT>(p.q, p.w, ks->row0, ks->nrows, qtile, wq, tid - 32, kThreads - 32);
+        fence_proxy_async_smem();
+        asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");
+    }
 
     // ------------------------------------------------------------ main loop
     if (warp == 0 && lane == 0) {
@@ -455,16 +473,35 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
             t_loc = ks->sel.bnd.bin;
         }
         // global bound: bin of the k-th best candidate published so far by
-        // other chunks of this sequence (a lower bound on the final k-th score)
-        uint32_t* gcopy = reinterpret_cast<uint32_t*>(a_tiles);
-        for (int i = tid; i < kHistBins; i += kThreads) gcopy[i] = __ldcg(gh + i);
-        __syncthreads();
-        block_find_suffix(gcopy, kHistBins, static_cast<uint32_t>(k), ks->sel.scratch, &ks->sel.bnd);
-        const int t_glob = ks->sel.bnd.bin < 0 ? 0 : ks->sel.bnd.bin;
+        // other chunks of this sequence (a lower bound on the final k-th
+        // score); only worth the read when the sequence has several chunks
+        int t_glob = 0;
+        if (nch > 2) {
+            uint32_t* gcopy = reinterpret_cast<uint32_t*>(a_tiles);
+            copy_hist_global(gcopy, gh);
+            __syncthreads();
+            block_find_suffix(gcopy, kHistBins, static_cast<uint32_t>(k), ks->sel.scratch, &ks->sel.bnd);
+            t_glob = ks->sel.bnd.bin < 0 ? 0 : ks->sel.bnd.bin;
+        }
         const int T = max(t_loc, t_glob);
-        // publish every score in bins >= T
-        const int64_t unit = static_cast<int64_t>(b) * p.max_chunks + c;
-        uint64_t* cl = p.cand + unit * p.chunk;
+        // every score in bins >= T is published: reserve that many slots in the
+        // sequence's candidate buffer with one atomic, then write them
+        {
+            uint32_t mine = 0;
+            for (int i = tid * (kHistBins / kThreads); i < (tid + 1) * (kHistBins / kThreads); ++i)
+                if (i >= T) mine += hist[i];
+            for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+            if (lane == 0) ks->sel.scratch[warp] = mine;
+            __syncthreads();
+            if (tid == 0) {
+                uint32_t tot = 0;
+                for (int w8 = 0; w8 < kThreads / 32; ++w8) tot += ks->sel.scratch[w8];
+                ks->ncand = 0;
+                ks->ticket = atomicAdd(p.seqcnt + b, tot);   // base slot of this chunk
+            }
+            __syncthreads();
+        }
+        uint64_t* cl = p.cand + static_cast<int64_t>(b) * p.cand_cap + ks->ticket;
         const int nround = (n + kThreads - 1) / kThreads * kThreads;
         for (int i = tid; i < nround; i += kThreads) {
             uint32_t kk = 0;
@@ -473,18 +510,13 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
                 kk = score_key(cscores[i]);
                 take = static_cast<int>(key_bin(kk)) >= T;
             }
-            const unsigned m = __ballot_sync(0xffffffffu, take);
-            uint32_t base = 0;
-            if (lane == 0 && m) base = atomicAdd(&ks->ncand, static_cast<uint32_t>(__popc(m)));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if (take) cl[base + __popc(m & ((1u << lane) - 1u))] = make_comp(kk, key_begin + i);
+            warp_append(cl, &ks->ncand, 0xFFFFFFFFu, make_comp(kk, key_begin + i), take);
         }
         for (int i = tid; i < kHistBins; i += kThreads)
             if (i >= T && hist[i]) atomicAdd(gh + i, hist[i]);
         __threadfence();
         __syncthreads();
         if (tid == 0) {
-            p.cnt[unit] = ks->ncand;
             if (ks->bad || ks->abort) atomicOr(p.seqflag + b, 1u);
             __threadfence();
             ks->ticket = atomicAdd(p.ctr + b, 1u);
@@ -494,8 +526,9 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
 
         // ------------------------------------------------ sequence merge (last chunk)
         __threadfence();
-        for (int i = tid; i < kHistBins; i += kThreads) hist[i] = __ldcg(gh + i);
+        copy_hist_global(hist, gh);
         const uint32_t flagged = __ldcg(p.seqflag + b);
+        const uint32_t total = __ldcg(p.seqcnt + b);
         __syncthreads();
         int32_t* oi = p.out_idx + static_cast<int64_t>(b) * k;
         float* os = p.out_score ? p.out_score + static_cast<int64_t>(b) * k : nullptr;
@@ -508,22 +541,20 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
             uint64_t* sel = reinterpret_cast<uint64_t*>(a_tiles);
             uint64_t* bndbuf = sel + IDX_MAX_TOPK;
             const int bcap = (kStages * plan.a_stage_bytes - IDX_MAX_TOPK * 8) / 8;
-            const int64_t ubase = static_cast<int64_t>(b) * p.max_chunks;
-            auto each = [&](auto f) {
-                for (int cc = 0; cc < nch; ++cc) {
-                    const uint32_t cn = __ldcg(p.cnt + ubase + cc);
-                    const uint64_t* L = p.cand + (ubase + cc) * p.chunk;
-                    for (uint32_t j = tid; j < cn; j += kThreads) f(__ldcg(reinterpret_cast<const unsigned long long*>(L) + j));
-                }
-            };
+            const uint64_t* L = p.cand + static_cast<int64_t>(b) * p.cand_cap;
+            auto each = [&](auto f) { walk_global(L, total, f); };
             select_topk_from_hist(each, hist, k, sel, bndbuf, bcap, &ks->sel, oi, os);
         }
         // leave the per-sequence state zeroed for the next call
         __syncthreads();
-        for (int i = tid; i < kHistBins; i += kThreads) gh[i] = 0;
+        reinterpret_cast<uint4*>(gh)[tid] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(gh)[tid + 256] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(gh)[tid + 512] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(gh)[tid + 768] = make_uint4(0, 0, 0, 0);
         if (tid == 0) {
             p.ctr[b] = 0;
             p.seqflag[b] = 0;
+            p.seqcnt[b] = 0;
         }
     }
 }

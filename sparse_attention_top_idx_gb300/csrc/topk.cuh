@@ -104,11 +104,85 @@ struct SelectSmem {
     uint64_t thr;        // composite threshold of the boundary refinement
 };
 
+// Append c to buf (shared counter *cnt, capacity cap) for the lanes with
+// `take`; one shared atomic per warp.  Every lane of the warp must call it.
+// The counter still advances past cap, so callers can detect overflow.
+__device__ __forceinline__ void warp_append(uint64_t* buf, uint32_t* cnt, uint32_t cap, uint64_t c,
+                                            bool take) {
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    if (m == 0u) return;
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(m) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(cnt, static_cast<uint32_t>(__popc(m)));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    const uint32_t pos = base + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
+    if (take && pos < cap) buf[pos] = c;
+}
+
+// Candidate walks.  A walk `each(f)` calls f(comp, valid) for every candidate,
+// strided over the block's 256 threads, with the same number of calls in every
+// lane of a warp (lanes past the end get valid = false), so f may use warp
+// collectives.
+
+// A shared-memory array of n composites.
+template <class F>
+__device__ __forceinline__ void walk_smem(const uint64_t* a, uint32_t n, F f) {
+    for (uint32_t b0 = 0; b0 < n; b0 += kTopkThreads) {
+        const uint32_t i = b0 + threadIdx.x;
+        const bool v = i < n;
+        f(v ? a[i] : 0ull, v);
+    }
+}
+
+// A global array of n composites, eight independent loads in flight per thread.
+template <class F>
+__device__ __forceinline__ void walk_global(const uint64_t* a, uint32_t n, F f) {
+    constexpr uint32_t U = 8;
+    const unsigned long long* p = reinterpret_cast<const unsigned long long*>(a);
+    for (uint32_t b0 = 0; b0 < n; b0 += kTopkThreads * U) {
+        unsigned long long v[U];
+#pragma unroll
+        for (uint32_t u = 0; u < U; ++u) {
+            const uint32_t i = b0 + u * kTopkThreads + threadIdx.x;
+            v[u] = (i < n) ? __ldcg(p + i) : 0ull;
+        }
+#pragma unroll
+        for (uint32_t u = 0; u < U; ++u) {
+            const uint32_t i = b0 + u * kTopkThreads + threadIdx.x;
+            f(static_cast<uint64_t>(v[u]), i < n);
+        }
+    }
+}
+
+// A global row of n fp32 scores (16-byte aligned, readable up to n rounded up
+// to 4): candidate i is (score_key(row[i]), i).  Eight float4 loads in flight.
+template <class F>
+__device__ __forceinline__ void walk_row(const float* row, int n, F f) {
+    constexpr int U = 8;
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    for (int b0 = 0; b0 < n; b0 += kTopkThreads * 4 * U) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = b0 + (u * kTopkThreads + static_cast<int>(threadIdx.x)) * 4;
+            v[u] = (i < n) ? __ldcg(r4 + (i >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = b0 + (u * kTopkThreads + static_cast<int>(threadIdx.x)) * 4;
+            f(make_comp(score_key(v[u].x), i), i < n);
+            f(make_comp(score_key(v[u].y), i + 1), i + 1 < n);
+            f(make_comp(score_key(v[u].z), i + 2), i + 2 < n);
+            f(make_comp(score_key(v[u].w), i + 3), i + 3 < n);
+        }
+    }
+}
+
 // Exact refinement inside one bin: among the candidate set X (all composites
 // whose top 12 bits equal `bin`), find the composite threshold thr such that
-// exactly m members of X are >= thr.  `each(f)` must call f(comp) for every
-// candidate of the full set, strided over the block's threads (it may visit
-// composites outside X; they are filtered here).  Called by all 256 threads.
+// exactly m members of X are >= thr.  `each` walks a superset of X (members
+// outside X are filtered here).  Called by all 256 threads.
 template <class Each>
 __device__ uint64_t radix_refine(Each each, int bin, uint32_t m, SelectSmem* ss) {
     uint64_t prefix = static_cast<uint64_t>(bin) << 52;
@@ -120,8 +194,8 @@ __device__ uint64_t radix_refine(Each each, int bin, uint32_t m, SelectSmem* ss)
         const uint64_t dmask = (pass == 6) ? 0xFull : 0xFFull;
         ss->hist256[threadIdx.x] = 0;
         __syncthreads();
-        each([&](uint64_t c) {
-            if ((c & mask) == prefix) atomicAdd(&ss->hist256[(c >> sh) & dmask], 1u);
+        each([&](uint64_t c, bool v) {
+            hist_add_warp(ss->hist256, static_cast<uint32_t>((c >> sh) & dmask), v && (c & mask) == prefix);
         });
         __syncthreads();
         block_find_suffix(ss->hist256, 256, need, ss->scratch, &ss->bnd);
@@ -163,8 +237,7 @@ __device__ __forceinline__ int next_pow2(int x) {
 }
 
 // Final selection of one query row from a candidate set whose 4096-bin
-// histogram `hist` (shared) is exact.  `each(f)` visits every candidate
-// composite (strided over the block).  sel: shared buffer of >= next_pow2(k)
+// histogram `hist` (shared) is exact.  `each` walks every candidate.  sel: shared buffer of >= next_pow2(k)
 // composites; bndbuf: shared buffer of bcap composites.  Writes the k outputs
 // (descending, -1 / -inf padded).  Called by all 256 threads.
 template <class Each>
@@ -181,46 +254,29 @@ __device__ void select_topk_from_hist(Each each, const uint32_t* hist, int k, ui
     }
     __syncthreads();
     // gather: bins above the boundary go straight to sel, the boundary bin to bndbuf
-    each([&](uint64_t c) {
-        int b = static_cast<int>(comp_key(c) >> kHistShift);
-        if (b > bstar) {
-            uint32_t p = atomicAdd(&ss->nsel, 1u);
-            sel[p] = c;
-        } else if (b == bstar) {
-            uint32_t p = atomicAdd(&ss->nbnd, 1u);
-            if (p < static_cast<uint32_t>(bcap)) bndbuf[p] = c;
-        }
+    each([&](uint64_t c, bool v) {
+        const int b = static_cast<int>(comp_key(c) >> kHistShift);
+        warp_append(sel, &ss->nsel, static_cast<uint32_t>(k), c, v && b > bstar);
+        warp_append(bndbuf, &ss->nbnd, static_cast<uint32_t>(bcap), c, v && b == bstar);
     });
     __syncthreads();
     if (bstar >= 0) {
         const uint32_t m = static_cast<uint32_t>(k) - above;
         const uint32_t nb = ss->nbnd;
-        if (nb == m) {
+        const bool fits = nb <= static_cast<uint32_t>(bcap);
+        if (fits && nb == m) {
             for (uint32_t i = tid; i < nb; i += kTopkThreads) sel[above + i] = bndbuf[i];
         } else {
-            uint64_t thr;
-            if (nb <= static_cast<uint32_t>(bcap)) {
-                thr = radix_refine(
-                    [&](auto f) {
-                        for (uint32_t i = tid; i < nb; i += kTopkThreads) f(bndbuf[i]);
-                    },
-                    bstar, m, ss);
-            } else {
-                thr = radix_refine(each, bstar, m, ss);
-            }
+            auto each_bnd = [&](auto f) { walk_smem(bndbuf, nb, f); };
+            const uint64_t thr = fits ? radix_refine(each_bnd, bstar, m, ss) : radix_refine(each, bstar, m, ss);
             if (tid == 0) ss->nsel = above;
             __syncthreads();
-            if (nb <= static_cast<uint32_t>(bcap)) {
-                for (uint32_t i = tid; i < nb; i += kTopkThreads) {
-                    uint64_t c = bndbuf[i];
-                    if (c >= thr) sel[atomicAdd(&ss->nsel, 1u)] = c;
-                }
-            } else {
-                each([&](uint64_t c) {
-                    if (static_cast<int>(comp_key(c) >> kHistShift) == bstar && c >= thr)
-                        sel[atomicAdd(&ss->nsel, 1u)] = c;
-                });
-            }
+            auto take = [&](uint64_t c, bool v) {
+                const bool in = v && static_cast<int>(comp_key(c) >> kHistShift) == bstar && c >= thr;
+                warp_append(sel, &ss->nsel, static_cast<uint32_t>(k), c, in);
+            };
+            if (fits) each_bnd(take);
+            else each(take);
         }
         __syncthreads();
     }

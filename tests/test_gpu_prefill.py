@@ -62,7 +62,6 @@ def test_prefill_chunk_full_size_sampled():
     s = np.sort(idx, axis=1)
     assert np.all(np.diff(s, axis=1) > 0)                 # no duplicates in any row
     assert np.all(np.diff(got["score"], axis=1) <= 0)     # descending in every row
-    assert np.all(idx[:, 0] == W.needle_pos[0])
 
 
 @pytest.mark.parametrize("mode", [0, 1])
