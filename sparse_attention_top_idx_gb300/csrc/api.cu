@@ -48,21 +48,19 @@ bool same_device(const idx_cache* c) {
 struct DecodeWs {
     size_t ctr, ghist, seqflag, seqcnt, cand, total;
     int64_t cand_cap;
-    int chunk, max_chunks;
+    dsaidx::DecodeGeom geom;
 };
 DecodeWs decode_ws(const idx_cache* c, int batch, int max_seq_len) {
     DecodeWs w{};
-    w.chunk = dsaidx::decode_chunk(c, batch, max_seq_len);
-    w.max_chunks = max_seq_len > 0 ? (max_seq_len + w.chunk - 1) / w.chunk : 1;
+    w.geom = dsaidx::decode_geometry(c, batch, max_seq_len);
     const size_t nb = static_cast<size_t>(batch);
-    const size_t units = nb * static_cast<size_t>(w.max_chunks);
+    w.cand_cap = static_cast<int64_t>(w.geom.nseg_max) * w.geom.cluster * w.geom.chunk;
     size_t o = dsaidx::kWsHeaderBytes;
     w.ctr = o;      o = align_up(o + nb * 4, 256);
     w.ghist = o;    o = align_up(o + nb * dsaidx::kHistBins * 4, 256);
     w.seqflag = o;  o = align_up(o + nb * 4, 256);
     w.seqcnt = o;   o = align_up(o + nb * 4, 256);
-    w.cand_cap = static_cast<int64_t>(w.max_chunks) * w.chunk;
-    w.cand = o;     o = align_up(o + units * static_cast<size_t>(w.chunk) * 8, 256);
+    w.cand = o;     o = align_up(o + nb * static_cast<size_t>(w.cand_cap) * 8, 256);
     w.total = o;
     return w;
 }
@@ -176,12 +174,13 @@ idx_status idx_score_topk_decode(const idx_cache* cache, const void* q_bf16_dev,
     if (batch == 0) return IDX_OK;
     if (!q_bf16_dev || !w_dev || !block_table_dev || !seq_lens_dev || !out_idx_dev || !workspace_dev)
         return IDX_ERR_INVALID_ARG;
-    if (!aligned(q_bf16_dev, 16) || !aligned(w_dev, 4) || !aligned(workspace_dev, 256))
+    if (!aligned(q_bf16_dev, 16) || !aligned(w_dev, 16) || !aligned(workspace_dev, 256))
         return IDX_ERR_INVALID_ARG;
     if (!same_device(cache)) return IDX_ERR_INVALID_ARG;
     const DecodeWs ws = decode_ws(cache, batch, max_seq_len);
     if (ws_bytes < ws.total) return IDX_ERR_WORKSPACE_TOO_SMALL;
-    if (static_cast<int64_t>(batch) * ws.max_chunks >= (int64_t(1) << 31)) return IDX_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(batch) * ws.geom.nseg_max * ws.geom.cluster >= (int64_t(1) << 31))
+        return IDX_ERR_INVALID_ARG;
     uint8_t* base = static_cast<uint8_t*>(workspace_dev);
     dsaidx::ScoreParams p{};
     p.q = static_cast<const uint16_t*>(q_bf16_dev);
@@ -195,8 +194,9 @@ idx_status idx_score_topk_decode(const idx_cache* cache, const void* q_bf16_dev,
     p.batch = batch;
     p.max_seq_len = max_seq_len;
     p.topk = topk;
-    p.chunk = ws.chunk;
-    p.max_chunks = ws.max_chunks;
+    p.chunk = ws.geom.chunk;
+    p.cluster = ws.geom.cluster;
+    p.nseg_max = ws.geom.nseg_max;
     p.out_idx = out_idx_dev;
     p.out_score = out_score_dev;
     p.status = reinterpret_cast<int32_t*>(base);
@@ -231,7 +231,7 @@ idx_status idx_score_topk_prefill(const idx_cache* cache, const void* q_bf16_dev
     if (!q_bf16_dev || !w_dev || !cu_seqlens_q_dev || !seq_lens_dev || !block_table_dev || !out_idx_dev ||
         !workspace_dev)
         return IDX_ERR_INVALID_ARG;
-    if (!aligned(q_bf16_dev, 16) || !aligned(w_dev, 4) || !aligned(workspace_dev, 256))
+    if (!aligned(q_bf16_dev, 16) || !aligned(w_dev, 16) || !aligned(workspace_dev, 256))
         return IDX_ERR_INVALID_ARG;
     if (!same_device(cache)) return IDX_ERR_INVALID_ARG;
     const PrefillWs ws = prefill_ws(total_q, max_seq_len);
@@ -251,7 +251,8 @@ idx_status idx_score_topk_prefill(const idx_cache* cache, const void* q_bf16_dev
     p.max_seq_len = max_seq_len;
     p.topk = topk;
     p.chunk = 0;
-    p.max_chunks = 0;
+    p.cluster = 1;
+    p.nseg_max = 0;
     p.total_q = total_q;
     p.num_groups = (total_q + dsaidx::kPrefillQT - 1) / dsaidx::kPrefillQT + batch;
     p.out_idx = out_idx_dev;

@@ -51,6 +51,37 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 }
 
 // ---------------------------------------------------------------------------
+// x / s rounded to nearest even, for many x over one divisor s (a normal,
+// positive fp32).  Markstein's division: with y = RN(1/s), q = RN(x * y) is
+// within one ulp of x / s, the remainder r = x - q * s is exact under FMA, and
+// RN(q + r * y) is the correctly rounded quotient (P. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990), as long as s and 1 / s are normal and the quotient is
+// normal.  The callers divide by amax / 448, so |x / s| <= 448; a quotient
+// below the normal range (x some 2^-133 times the row's largest magnitude)
+// may come out one subnormal ulp off, which cannot change its e4m3 code (0
+// with the sign of x).  Divisors below 2^-125 use the IEEE division itself.
+// ---------------------------------------------------------------------------
+struct DivBy {
+    float s, y;
+    bool fast;
+    __device__ __forceinline__ explicit DivBy(float s_)
+        : s(s_), y(0.0f), fast(s_ >= 0x1p-125f && s_ <= 0x1p125f) {
+#ifdef __CUDA_ARCH__
+        y = __frcp_rn(s_);
+#endif
+    }
+    __device__ __forceinline__ float operator()(float x) const {
+        if (!fast) return __fdiv_rn(x, s);
+        const float q = __fmul_rn(x, y);
+        const float r = __fmaf_rn(-q, s, x);
+        // r = 0: q is exact (and keeps the sign of a zero x, which the
+        // correction step would turn into +0)
+        return (r == 0.0f) ? q : __fmaf_rn(r, y, q);
+    }
+};
+
+// ---------------------------------------------------------------------------
 // shared-memory addresses, fences, timers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -113,6 +144,69 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
             }
         }
     }
+}
+
+// Bounded wait that also acquires at cluster scope: writes another CTA of the
+// cluster made before a release-arrive on this barrier are visible after it.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int32_t* status) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    unsigned long long t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+            set_status(status, IDX_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// thread-block clusters: rank, barrier, distributed shared memory
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Whole-cluster barrier; every thread of every CTA of the cluster must reach
+// it (used once, at kernel start, before any CTA can leave).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void dsmem_red_add(uint32_t addr, uint32_t v) {
+    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void dsmem_st_u64(uint32_t addr, uint64_t v) {
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+// Release-arrive on an mbarrier of any CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 
 // ---------------------------------------------------------------------------

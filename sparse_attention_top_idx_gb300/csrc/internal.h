@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "dsaidx.h"
 
 struct idx_cache {
@@ -40,8 +42,9 @@ struct ScoreParams {
     int batch;
     int max_seq_len;
     int topk;
-    int chunk;                   // decode: keys per CTA (multiple of 128)
-    int max_chunks;              // decode: ceil(max_seq_len / chunk)
+    int chunk;                   // decode: largest chunk of keys per CTA (multiple of 128)
+    int cluster;                 // decode: CTAs per cluster (one sequence segment)
+    int nseg_max;                // decode: segments of the longest sequence
     int total_q;                 // prefill
     int num_groups;              // prefill: grid bound on query groups
     int32_t* out_idx;
@@ -53,7 +56,7 @@ struct ScoreParams {
     uint32_t* seqflag;           // decode: [batch] device-check flags
     uint32_t* seqcnt;            // decode: [batch] candidates published per sequence
     uint64_t* cand;              // decode: [batch, cand_cap] composites
-    int64_t cand_cap;            // decode: max_chunks * chunk (>= every seq_len)
+    int64_t cand_cap;            // decode: nseg_max * cluster * chunk (>= every seq_len)
     float* scores;               // prefill: [total_q, score_stride]
     int64_t score_stride;
     uint32_t* rowflag;           // prefill: [total_q]
@@ -62,27 +65,47 @@ struct ScoreParams {
 // Shared-memory plan of the scoring kernel for (fp8, queries per CTA, chunk).
 struct SmemPlan {
     int stages, a_stage_bytes, q_bytes, n_cols;
-    int a_off, q_off, scale_off, w_off, hist_off, scores_off, misc_off, bar_off;
+    int a_off, q_off, scale_off, w_off, hist_off, raw_off, misc_off, bar_off;
     int total;   // bytes to request (includes 1 KB of alignment slack)
 };
 
+// Decode keeps two CTAs per SM (<= ~111 KB each for fp8 keys): four key stages
+// while the chunk's scores take <= 16 KB, three for larger chunks.  The raw
+// query rows are staged where the decode scores later go (or, for prefill,
+// in a 64 KB region of their own).
 __host__ __device__ inline SmemPlan make_plan(bool fp8, int qt, int chunk) {
     SmemPlan p{};
     p.n_cols = 64 * qt;
-    p.stages = (qt == 1) ? (fp8 ? 3 : 2) : (fp8 ? 4 : 2);
+    p.stages = (qt == 1) ? (fp8 ? (chunk <= 4096 ? 4 : 3) : 2) : (fp8 ? 4 : 2);
     p.a_stage_bytes = fp8 ? 16384 : 32768;
     p.q_bytes = p.n_cols * (fp8 ? 128 : 256);
+    const int raw_bytes = (qt == 1) ? (chunk * 4 > 16384 ? chunk * 4 : 16384) : qt * 16384;
     int o = 0;
     p.a_off = o;       o += p.stages * p.a_stage_bytes;
     p.q_off = o;       o += p.q_bytes;
     p.scale_off = o;   o += fp8 ? p.stages * 512 : 0;
     p.w_off = o;       o += p.n_cols * 4;
     p.hist_off = o;    o += (qt == 1) ? 4096 * 4 : 0;
-    p.scores_off = o;  o += (qt == 1) ? chunk * 4 : 0;
+    p.raw_off = o;     o += raw_bytes;
     p.misc_off = o;    o += 4096;            // selection scratch, flags, group scan
     p.bar_off = o;     o += 256;             // mbarriers
     p.total = o + 1024;
     return p;
+}
+
+// Raise a kernel's dynamic shared-memory limit to `bytes`, once per device
+// (the first call for each device sets it; later calls, including calls made
+// while a stream is being captured into a graph, skip the runtime call).
+template <class Kern>
+inline cudaError_t set_smem_once(Kern kern, int bytes, std::atomic<unsigned long long>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
 }
 
 // Kernel launchers (one per translation unit).
@@ -91,7 +114,11 @@ cudaError_t launch_store(const idx_cache* c, const void* k, const int64_t* slots
 cudaError_t launch_decode(const idx_cache* c, const ScoreParams& p, cudaStream_t st);
 cudaError_t launch_prefill(const idx_cache* c, const ScoreParams& p, cudaStream_t st);
 
-// Decode chunk size (keys per CTA) for a batch shape on a device.
-int decode_chunk(const idx_cache* c, int batch, int max_seq_len);
+// Decode geometry for a batch shape: clusters of `cluster` CTAs, each CTA
+// scoring at most `chunk` keys, `nseg_max` cluster segments per sequence.
+struct DecodeGeom {
+    int cluster, chunk, nseg_max;
+};
+DecodeGeom decode_geometry(const idx_cache* c, int batch, int max_seq_len);
 
 }  // namespace dsaidx

@@ -29,7 +29,6 @@ __global__ void __launch_bounds__(kTopkThreads) prefill_select_kernel(const Scor
     const SelectPlan sp = select_plan();
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + sp.hist_off);
     uint64_t* sel = reinterpret_cast<uint64_t*>(smem + sp.sel_off);
-    uint64_t* bndbuf = reinterpret_cast<uint64_t*>(smem + sp.bnd_off);
     SelectSmem* ss = reinterpret_cast<SelectSmem*>(smem + sp.ss_off);
     __shared__ int s_nvis, s_bad;
     const int r = blockIdx.x;
@@ -68,14 +67,16 @@ __global__ void __launch_bounds__(kTopkThreads) prefill_select_kernel(const Scor
     auto each = [&](auto f) { walk_row(row, nvis, f); };
     each([&](uint64_t c, bool v) { hist_add_warp(hist, key_bin(comp_key(c)), v); });
     __syncthreads();
-    select_topk_from_hist(each, hist, p.topk, sel, bndbuf, kSelBcap, ss, oi, os);
+    select_topk_from_hist<16>(each, hist, p.topk, sel, IDX_MAX_TOPK + kSelBcap, ss, oi, os);
 }
 
 template <bool kFp8, int kBs>
 cudaError_t launch_prefill_t(const idx_cache* c, const ScoreParams& p, cudaStream_t st) {
+    static std::atomic<unsigned long long> attr_done{0};
+    static std::atomic<unsigned long long> sel_attr_done{0};
     const SmemPlan plan = make_plan(kFp8, kPrefillQT, 0);
     auto kern = score_kernel<kFp8, kBs, kPrefillQT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.total);
+    cudaError_t e = set_smem_once(kern, plan.total, attr_done);
     if (e != cudaSuccess) return e;
     if (p.num_groups > 0) {
         kern<<<p.num_groups, kThreads, plan.total, st>>>(c->tmap, p);
@@ -83,7 +84,7 @@ cudaError_t launch_prefill_t(const idx_cache* c, const ScoreParams& p, cudaStrea
         if (e != cudaSuccess) return e;
     }
     const SelectPlan sp = select_plan();
-    e = cudaFuncSetAttribute(prefill_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sp.total);
+    e = set_smem_once(prefill_select_kernel, sp.total, sel_attr_done);
     if (e != cudaSuccess) return e;
     prefill_select_kernel<<<p.total_q, kTopkThreads, sp.total, st>>>(p);
     return cudaGetLastError();

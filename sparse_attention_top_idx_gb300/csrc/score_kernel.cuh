@@ -8,9 +8,12 @@
 // it: straight from the paged blocks through the block table.
 //
 // One CTA of 256 threads (8 warps) per work unit:
-//   decode  (kQT = 1): one sequence, one chunk of its keys; N = 64 heads.
+//   decode  (kQT = 1): a chunk of one sequence's keys against its 64 query
+//                      heads (N = 64); the CTAs of a sequence segment form a
+//                      thread-block cluster that selects the top-k together;
 //   prefill (kQT = 4): up to 4 consecutive query rows of one sequence against
-//                      every key they can see; N = 4 * 64 = 256.
+//                      every key they can see (N = 256); scores go to the
+//                      workspace for the row select kernel.
 // The contraction D[s, (t, h)] = sum_d k[s, d] q[t, h, d] runs on the 5th-gen
 // tensor cores: M = 128 keys (A, K-major, TMA-loaded 64- or 32-row boxes of the
 // paged blocks, 128-byte swizzle), N = 64 * kQT query-heads (B, quantised by
@@ -18,9 +21,10 @@
 // (two buffers so the epilogue of tile i overlaps the MMA of tile i + 1).
 // fp8 keys use kind::f8f6f4 (e4m3 x e4m3), bf16 keys kind::f16.
 //
-// Warp roles in the main loop: warp 0 lane 0 issues TMA, warp 1 owns TMEM and
-// lane 0 issues MMAs, warps 4..7 (TMEM lane quadrants 0..3, one key row per
-// thread) run the epilogue: ks[s] * sum_h w'[t, h] * max(D, 0).
+// Warp roles: warp 0 lane 0 issues the bulk copy of the query rows and then
+// the key TMA; warps 1..7 quantise the queries into the B tile; warp 1 owns
+// TMEM and its lane 0 issues the MMAs; warps 4..7 (TMEM lane quadrants 0..3,
+// one key row per thread) run the epilogue ks[s] * sum_h w'[t, h] * max(D, 0).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -31,13 +35,22 @@
 
 namespace dsaidx {
 
+// Decode selection modes chosen by a cluster's leader.
+constexpr uint32_t kModeSmem = 1;     // candidates pushed into the leader's shared memory
+constexpr uint32_t kModeGlobal = 2;   // candidates published to the workspace
+
 struct KernelShared {
     uint32_t tmem_base;
     int abort;          // a role gave up on a bounded wait
     int bad;            // a block id failed its check
-    uint32_t ncand;
+    uint32_t ncand;     // leader: candidates received in shared memory
     uint32_t ticket;
-    int unit_b, unit_c, key_begin, key_end, seq_len, nrows, row0;
+    int unit_b, key_begin, key_end, seq_len, nrows, row0, nq;
+    int seg, nseg;      // decode: segment of the sequence and segments in it
+    int cl_bin;         // decode: boundary bin broadcast by the cluster leader
+    uint32_t cl_mode;   // decode: selection mode broadcast by the leader
+    uint32_t cl_count;  // decode: candidates at or above the boundary (leader)
+    uint32_t cl_flag;   // decode: a CTA of the segment failed a device check
     int pos[kPrefillQT];
     SelectSmem sel;
     uint32_t grp[kThreads];   // prefill: group-count scan
@@ -56,12 +69,6 @@ __device__ __forceinline__ int sw128_off(int r, int c) {
     return (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
 }
 
-// Quantise (fp8) or copy (bf16) the query rows of this CTA into the B operand
-// tile, and fill w'.  Row n = j * 64 + h (query j of the CTA, head h); rows of
-// missing queries (j >= nrows) get zero codes and zero weight.  fp8: per row
-// scale sq = amax / 448 (IEEE), codes e4m3(q / sq), w' = w * sq; amax = 0 gives
-// zero codes and w' = 0 * w.  Four consecutive threads per row (32 elements
-// each); t / nthreads: this thread's index among the nthreads doing the work.
 // Copy a 4096-bin histogram from global memory (bypassing L1) into shared
 // memory: four independent 16-byte loads per thread of a 256-thread block.
 __device__ __forceinline__ void copy_hist_global(uint32_t* dst, const uint32_t* src) {
@@ -74,33 +81,42 @@ __device__ __forceinline__ void copy_hist_global(uint32_t* dst, const uint32_t* 
     for (int u = 0; u < 4; ++u) d4[u * 256 + threadIdx.x] = v[u];
 }
 
+// Quantise (fp8) or copy (bf16) the CTA's query rows, staged in shared memory
+// as raw [nrows][64][128] bf16 with their head weights in wq, into the B
+// operand tile, and turn wq into w'.  Row n = j * 64 + h (query j, head h);
+// rows of missing queries (j >= nrows) get zero codes and zero weight.  fp8:
+// per row scale sq = amax / 448 (IEEE), codes e4m3(q / sq) with the quotient
+// correctly rounded, w' = w * sq; amax = 0 gives zero codes and w' = 0 * w.
+// Four consecutive threads per row (32 elements each); t / nthreads: this
+// thread's index among the nthreads doing the work.
 template <bool kFp8, int kQT>
-__device__ __forceinline__ void prep_queries(const uint16_t* __restrict__ q, const float* __restrict__ w,
-                             int row0, int nrows, uint8_t* qtile, float* wq, int t, int nthreads) {
+__device__ __forceinline__ void prep_queries(const uint8_t* raw, int nrows, uint8_t* qtile, float* wq,
+                                             int t, int nthreads) {
     constexpr int kRows = 64 * kQT;
     const int part = t & 3;
     const unsigned gmask = 0xFu << (threadIdx.x & 28);   // the 4 lanes sharing a row
     for (int r = t >> 2; r < kRows; r += nthreads / 4) {
-        const int j = r >> 6, h = r & 63;
+        const int j = r >> 6;
         const bool have = j < nrows;
         uint4 v[4];
         if (have) {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                q + (static_cast<int64_t>(row0 + j) * 64 + h) * kHeadDim + part * 32);
+            const uint4* src = reinterpret_cast<const uint4*>(raw + static_cast<size_t>(r) * 256 + part * 64);
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[i] = src[i];
         } else {
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[i] = make_uint4(0, 0, 0, 0);
         }
+        const float wv = have ? wq[r] : 0.0f;
+        __syncwarp(gmask);   // every lane of the row has read wq[r]
         if constexpr (!kFp8) {
-            // elements [32 part, 32 part + 32) = 64 bytes; half = part / 2, chunks
+            // elements [32 part, 32 part + 32) = 64 bytes: half part / 2, chunks
             // 4 * (part & 1) .. +3 of that half
             uint8_t* half = qtile + (part >> 1) * (kRows * 128);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 *reinterpret_cast<uint4*>(half + sw128_off(r, (part & 1) * 4 + i)) = v[i];
-            if (part == 0) wq[r] = have ? w[static_cast<int64_t>(row0 + j) * 64 + h] : 0.0f;
+            if (part == 0) wq[r] = wv;
         } else {
             float x[32];
 #pragma unroll
@@ -118,12 +134,13 @@ __device__ __forceinline__ void prep_queries(const uint16_t* __restrict__ q, con
             amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
             const float sq = __fdiv_rn(amax, 448.0f);
+            const DivBy div(sq);
             uint32_t c[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 if (amax != 0.0f) {
-                    const float y0 = __fdiv_rn(x[4 * i + 0], sq), y1 = __fdiv_rn(x[4 * i + 1], sq);
-                    const float y2 = __fdiv_rn(x[4 * i + 2], sq), y3 = __fdiv_rn(x[4 * i + 3], sq);
+                    const float y0 = div(x[4 * i + 0]), y1 = div(x[4 * i + 1]);
+                    const float y2 = div(x[4 * i + 2]), y3 = div(x[4 * i + 3]);
                     c[i] = cvt_e4m3x2_pair(y0, y1) | (cvt_e4m3x2_pair(y2, y3) << 16);
                 } else {
                     c[i] = 0;
@@ -132,10 +149,7 @@ __device__ __forceinline__ void prep_queries(const uint16_t* __restrict__ q, con
             // bytes [32 part, 32 part + 32) = chunks 2 part and 2 part + 1
             *reinterpret_cast<uint4*>(qtile + sw128_off(r, 2 * part)) = make_uint4(c[0], c[1], c[2], c[3]);
             *reinterpret_cast<uint4*>(qtile + sw128_off(r, 2 * part + 1)) = make_uint4(c[4], c[5], c[6], c[7]);
-            if (part == 0) {
-                const float wv = have ? w[static_cast<int64_t>(row0 + j) * 64 + h] : 0.0f;
-                wq[r] = wv * sq;
-            }
+            if (part == 0) wq[r] = wv * sq;
         }
     }
 }
@@ -148,6 +162,8 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
     constexpr int kBlocksPerTile = kTileKeys / kBs;
     constexpr int kKSteps = kFp8 ? 4 : 8;
     constexpr uint32_t kBlockTx = kFp8 ? (kBs * 128 + kBs * 4) : (kBs * 256);
+    constexpr int kDecodeSortE = 8;                         // leader sorts up to 2048 candidates
+    constexpr uint32_t kDecodeSortCap = kTopkThreads * kDecodeSortE;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -159,7 +175,8 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
     float* scales = reinterpret_cast<float*>(smem + plan.scale_off);
     float* wq = reinterpret_cast<float*>(smem + plan.w_off);
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + plan.hist_off);
-    float* cscores = reinterpret_cast<float*>(smem + plan.scores_off);
+    uint8_t* raw = smem + plan.raw_off;                     // staged query rows (bf16)
+    float* cscores = reinterpret_cast<float*>(smem + plan.raw_off);   // decode: the chunk's scores
     KernelShared* ks = reinterpret_cast<KernelShared*>(smem + plan.misc_off);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
     uint64_t* full = bars;                 // [stages] TMA -> MMA
@@ -167,47 +184,49 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
     uint64_t* tfull = bars + 8;            // [2] MMA -> epilogue
     uint64_t* tempty = bars + 10;          // [2] epilogue -> MMA
     uint64_t* mdone = bars + 12;           // MMA drain at exit
+    uint64_t* qbar = bars + 13;            // query rows staged
+    uint64_t* hbar = bars + 14;            // decode leader: every CTA's histogram added
+    uint64_t* bbar = bars + 15;            // decode: boundary bin broadcast received
+    uint64_t* gbar = bars + 16;            // decode leader: every CTA's candidates pushed
 
     const int tid = threadIdx.x;
     const int warp = warp_id(), lane = lane_id();
     int32_t* status = p.status;
 
     // ------------------------------------------------------------ work unit
-    if (tid == 0) {
-        ks->abort = 0;
-        ks->bad = 0;
-        ks->ncand = 0;
-    }
     if constexpr (kDecode) {
-        const int b = blockIdx.x / p.max_chunks;
-        const int c = blockIdx.x - b * p.max_chunks;
+        // cluster (b, seg) of p.cluster CTAs; CTA `rank` takes the rank-th chunk
+        // of the segment.  Every CTA of a cluster sees the same (b, seg).
+        const int CL = p.cluster;
+        const int rank = static_cast<int>(cluster_rank());
+        const int cid = blockIdx.x / CL;
+        const int b = cid / p.nseg_max;
+        const int seg = cid - b * p.nseg_max;
         const int S = p.seq_lens[b];
-        if (S < 0 || S > p.max_seq_len) {
-            if (c == 0) {
-                if (tid == 0) set_status(status, IDX_ERR_DEVICE_CHECK);
+        const bool valid = S >= 0 && S <= p.max_seq_len;
+        int chunk = kTileKeys, nseg = 0;
+        if (valid && S > 0) {
+            chunk = min(p.chunk, ((S + CL - 1) / CL + kTileKeys - 1) / kTileKeys * kTileKeys);
+            nseg = (S + CL * chunk - 1) / (CL * chunk);
+        }
+        if (!(valid && S > 0)) {
+            if (seg == 0 && rank == 0) {
+                if (!valid && tid == 0) set_status(status, IDX_ERR_DEVICE_CHECK);
                 for (int j = tid; j < p.topk; j += kThreads) {
                     p.out_idx[static_cast<int64_t>(b) * p.topk + j] = -1;
                     if (p.out_score) p.out_score[static_cast<int64_t>(b) * p.topk + j] = -INFINITY;
                 }
             }
-            return;
+            return;   // the whole cluster leaves together
         }
-        const int nch = (S + p.chunk - 1) / p.chunk;
-        if (S == 0) {
-            if (c == 0)
-                for (int j = tid; j < p.topk; j += kThreads) {
-                    p.out_idx[static_cast<int64_t>(b) * p.topk + j] = -1;
-                    if (p.out_score) p.out_score[static_cast<int64_t>(b) * p.topk + j] = -INFINITY;
-                }
-            return;
-        }
-        if (c >= nch) return;
+        if (seg >= nseg) return;   // the whole cluster leaves together
         if (tid == 0) {
             ks->unit_b = b;
-            ks->unit_c = c;
+            ks->seg = seg;
+            ks->nseg = nseg;
             ks->seq_len = S;
-            ks->key_begin = c * p.chunk;
-            ks->key_end = min(S, (c + 1) * p.chunk);
+            ks->key_begin = min(S, seg * CL * chunk + rank * chunk);
+            ks->key_end = min(S, ks->key_begin + chunk);
             ks->row0 = b;
             ks->nrows = 1;
         }
@@ -232,16 +251,14 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
                 ks->grp[i] = acc;   // exclusive prefix
                 acc += v;
             }
-            ks->unit_b = -1;
-            if (static_cast<uint32_t>(g) < acc) ks->unit_b = -2;
+            ks->unit_b = (static_cast<uint32_t>(g) < acc) ? -2 : -1;
         }
         __syncthreads();
         if (ks->unit_b == -1) return;
-        // the thread whose range holds g finds the sequence
         {
+            // the thread whose range holds g finds the sequence
             const uint32_t lo = ks->grp[tid];
-            const uint32_t hi = lo + mine;
-            if (mine > 0 && static_cast<uint32_t>(g) >= lo && static_cast<uint32_t>(g) < hi) {
+            if (mine > 0 && static_cast<uint32_t>(g) >= lo && static_cast<uint32_t>(g) < lo + mine) {
                 uint32_t acc = lo;
                 for (int i = 0; i < per; ++i) {
                     const int bb = tid * per + i;
@@ -252,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
                         const int i0 = (g - static_cast<int>(acc)) * kQT;
                         const int S = p.seq_lens[bb];
                         ks->unit_b = bb;
-                        ks->unit_c = nq;
+                        ks->nq = nq;
                         ks->row0 = p.cu_q[bb] + i0;
                         ks->nrows = min(kQT, nq - i0);
                         ks->seq_len = S;
@@ -267,8 +284,7 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
         }
         __syncthreads();
         const int S = ks->seq_len;
-        const bool invalid = S > p.max_seq_len || ks->unit_c > S;   // unit_c holds nq here
-        if (invalid) {
+        if (S > p.max_seq_len || ks->nq > S) {
             if (tid == 0) set_status(status, IDX_ERR_DEVICE_CHECK);
             if (tid < ks->nrows) atomicOr(&p.rowflag[ks->row0 + tid], 1u);
             return;
@@ -277,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
     __syncthreads();
 
     const int key_begin = ks->key_begin, key_end = ks->key_end, seq_b = ks->unit_b;
-    const int ntiles = (key_end - key_begin + kTileKeys - 1) / kTileKeys;
+    const int ntiles = key_end > key_begin ? (key_end - key_begin + kTileKeys - 1) / kTileKeys : 0;
 
     // ------------------------------------------------------------ set-up
     if (tid == 0) {
@@ -290,7 +306,17 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
             mbar_init(&tempty[a], 4);
         }
         mbar_init(mdone, 1);
+        mbar_init(qbar, 1);
+        if constexpr (kDecode) {
+            mbar_init(hbar, p.cluster * kThreads);
+            mbar_init(bbar, 1);
+            mbar_init(gbar, p.cluster * kThreads);
+        }
         fence_mbar_init();
+        ks->abort = 0;
+        ks->bad = 0;
+        ks->ncand = 0;
+        ks->cl_flag = 0;
     }
     if (warp == 1) {
         tmem_alloc(&ks->tmem_base, 2 * kN);
@@ -302,18 +328,31 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // every CTA of the cluster has its barriers and histogram ready before any
+    // CTA touches another's shared memory
+    if constexpr (kDecode) cluster_sync_all();
     const uint32_t tmem = ks->tmem_base;
-    // Warp 0 starts streaming keys at once; warps 1..7 build the query tile
-    // meanwhile and meet on a named barrier before the first MMA.
+
+    // Warp 0 stages the query rows and starts streaming keys at once; warps
+    // 1..7 build the query tile meanwhile and meet on a named barrier before
+    // the first MMA.
     if (warp != 0) {
-        prep_queries<kFp8, kQT>(p.q, p.w, ks->row0, ks->nrows, qtile, wq, tid - 32, kThreads - 32);
+        if (!__all_sync(0xffffffffu, mbar_wait(qbar, 0, status, &ks->abort))) ks->abort = 1;
+        prep_queries<kFp8, kQT>(raw, ks->nrows, qtile, wq, tid - 32, kThreads - 32);
         fence_proxy_async_smem();
         asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");
     }
 
     // ------------------------------------------------------------ main loop
     if (warp == 0 && lane == 0) {
-        // TMA producer
+        // query rows (bf16) and their head weights, one bulk copy each
+        const uint64_t pol_q = policy_evict_first();
+        const int nrows = ks->nrows;
+        mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(nrows) * (64 * kHeadDim * 2 + 64 * 4));
+        bulk_load(raw, p.q + static_cast<int64_t>(ks->row0) * 64 * kHeadDim,
+                  static_cast<uint32_t>(nrows) * 64 * kHeadDim * 2, qbar, pol_q);
+        bulk_load(wq, p.w + static_cast<int64_t>(ks->row0) * 64, static_cast<uint32_t>(nrows) * 64 * 4, qbar, pol_q);
+        // TMA producer of the key tiles
         const uint64_t pol = kDecode ? policy_evict_first() : policy_evict_last();
         tma_prefetch_desc(&tmap);
         int t = 0;
@@ -358,11 +397,11 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
         // copies still in flight (only when a wait gave up) must land before exit
         for (int u = max(0, t - kStages); u < t; ++u)
             mbar_wait(&full[u % kStages], static_cast<uint32_t>(u / kStages) & 1u, status, nullptr);
+        mbar_wait(qbar, 0, status, nullptr);
     } else if (warp == 1 && lane == 0) {
         // MMA issuer
         constexpr uint32_t idesc = idesc_make(kFp8, kTileKeys, kN);
         const uint32_t q_base = smem_u32(qtile);
-        int issued = 0;
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % kStages;
             const uint32_t ph = static_cast<uint32_t>(t / kStages) & 1u;
@@ -390,12 +429,10 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
             }
             mma_commit(&empty[s]);
             mma_commit(&tfull[a]);
-            ++issued;
         }
         // every MMA issued above has finished once mdone completes
         mma_commit(mdone);
         mbar_wait(mdone, 0, status, nullptr);
-        (void)issued;
     } else if (warp >= 4) {
         // epilogue: one key row per thread
         const int qd = warp & 3;
@@ -458,51 +495,126 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
         }
         return;
     } else {
-        // ------------------------------------------------ chunk top-k candidates
+        // ------------------------------------------------ cluster top-k
+        // (1) the leader's histogram becomes the segment's histogram: every
+        //     other CTA adds its non-zero bins with DSMEM atomics.  (2) The
+        //     leader finds the boundary bin of the k-th best key and broadcasts
+        //     it.  (3) Every CTA pushes its keys at or above that bin into the
+        //     leader's shared memory, where one sort yields the top-k; or, for
+        //     sequences of several segments (or too many ties), publishes them
+        //     to the workspace and the last CTA of the sequence merges.
+        const int CL = p.cluster;
+        const uint32_t rank = cluster_rank();
         const int b = seq_b;
-        const int c = ks->unit_c;
-        const int S = ks->seq_len;
-        const int nch = (S + p.chunk - 1) / p.chunk;
         const int n = key_end - key_begin;
         const int k = p.topk;
-        uint32_t* gh = p.ghist + static_cast<int64_t>(b) * kHistBins;
-        // local bound: the chunk's own k-th best bin
-        int t_loc = 0;
-        if (n > k) {
+        if (rank != 0) {
+            const uint32_t lh = dsmem_addr(hist, 0);
+            for (int i = tid * (kHistBins / kThreads); i < (tid + 1) * (kHistBins / kThreads); ++i) {
+                const uint32_t v = hist[i];
+                if (v) dsmem_red_add(lh + 4u * static_cast<uint32_t>(i), v);
+            }
+        }
+        if (tid == 0 && (ks->bad || ks->abort)) dsmem_red_add(dsmem_addr(&ks->cl_flag, 0), 1u);
+        mbar_arrive_remote(dsmem_addr(hbar, 0));
+        if (rank == 0) {
+            if (!mbar_wait_cluster(hbar, 0, status)) ks->abort = 1;
             block_find_suffix(hist, kHistBins, static_cast<uint32_t>(k), ks->sel.scratch, &ks->sel.bnd);
-            t_loc = ks->sel.bnd.bin;
+            if (tid == 0) {
+                const uint32_t count_ge = ks->sel.bnd.above + ks->sel.bnd.at;
+                const uint32_t mode = (ks->nseg == 1 && count_ge <= kDecodeSortCap) ? kModeSmem : kModeGlobal;
+                ks->cl_count = count_ge;
+                for (int r = 0; r < CL; ++r) {
+                    dsmem_st_u32(dsmem_addr(&ks->cl_bin, static_cast<uint32_t>(r)), static_cast<uint32_t>(ks->sel.bnd.bin));
+                    dsmem_st_u32(dsmem_addr(&ks->cl_mode, static_cast<uint32_t>(r)), mode);
+                    mbar_arrive_remote(dsmem_addr(bbar, static_cast<uint32_t>(r)));
+                }
+            }
         }
-        // global bound: bin of the k-th best candidate published so far by
-        // other chunks of this sequence (a lower bound on the final k-th
-        // score); only worth the read when the sequence has several chunks
-        int t_glob = 0;
-        if (nch > 2) {
-            uint32_t* gcopy = reinterpret_cast<uint32_t*>(a_tiles);
-            copy_hist_global(gcopy, gh);
+        if (!mbar_wait_cluster(bbar, 0, status)) ks->abort = 1;
+        const int bstar = ks->cl_bin;            // -1: fewer than k keys in the segment
+        const uint32_t mode = ks->cl_mode;
+        const int nround = (n + kThreads - 1) / kThreads * kThreads;
+
+        if (mode == kModeSmem) {
+            const uint32_t lbuf = dsmem_addr(a_tiles, 0);
+            const uint32_t lcnt = dsmem_addr(&ks->ncand, 0);
+            for (int i = tid; i < nround; i += kThreads) {
+                uint32_t kk = 0;
+                bool take = false;
+                if (i < n) {
+                    kk = score_key(cscores[i]);
+                    take = static_cast<int>(key_bin(kk)) >= bstar;
+                }
+                const unsigned m = __ballot_sync(0xffffffffu, take);
+                if (m) {
+                    const int leader = __ffs(m) - 1;
+                    uint32_t base = 0;
+                    if (lane == leader) base = dsmem_atom_add(lcnt, static_cast<uint32_t>(__popc(m)));
+                    base = __shfl_sync(0xffffffffu, base, leader);
+                    if (take) {
+                        const uint32_t pos = base + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
+                        if (pos < kDecodeSortCap)
+                            dsmem_st_u64(lbuf + 8u * pos, make_comp(kk, key_begin + i));
+                    }
+                }
+            }
+            mbar_arrive_remote(dsmem_addr(gbar, 0));
+            if (rank != 0) return;   // nothing touches this CTA's shared memory any more
+            if (!mbar_wait_cluster(gbar, 0, status)) ks->abort = 1;
             __syncthreads();
-            block_find_suffix(gcopy, kHistBins, static_cast<uint32_t>(k), ks->sel.scratch, &ks->sel.bnd);
-            t_glob = ks->sel.bnd.bin < 0 ? 0 : ks->sel.bnd.bin;
+            int32_t* oi = p.out_idx + static_cast<int64_t>(b) * k;
+            float* os = p.out_score ? p.out_score + static_cast<int64_t>(b) * k : nullptr;
+            const int cnt = static_cast<int>(min(ks->cl_count, kDecodeSortCap));
+            if (ks->cl_flag || ks->abort) {
+                for (int j = tid; j < k; j += kThreads) {
+                    oi[j] = -1;
+                    if (os) os[j] = -INFINITY;
+                }
+                return;
+            }
+            uint64_t* buf = reinterpret_cast<uint64_t*>(a_tiles);
+            block_sort_desc_n<kDecodeSortE>(buf, cnt);
+            const int nsel = min(k, cnt);
+            for (int j = tid; j < k; j += kThreads) {
+                if (j < nsel) {
+                    const uint64_t c = buf[j];
+                    oi[j] = comp_index(c);
+                    if (os) os[j] = key_score(comp_key(c));
+                } else {
+                    oi[j] = -1;
+                    if (os) os[j] = -INFINITY;
+                }
+            }
+            return;
         }
-        const int T = max(t_loc, t_glob);
-        // every score in bins >= T is published: reserve that many slots in the
-        // sequence's candidate buffer with one atomic, then write them
+
+        // ------------------------------------------------ workspace path
+        // Publish every key in bins >= T (T: the segment's boundary bin, a lower
+        // bound on the sequence's k-th best) and its histogram counts, then the
+        // last CTA of the sequence selects from the published set.
+        const int T = max(bstar, 0);
+        uint32_t* gh = p.ghist + static_cast<int64_t>(b) * kHistBins;
+        const int nch = ks->nseg * CL;     // CTAs of the sequence
+        // count this CTA's keys in bins >= T (the leader's histogram holds the
+        // whole segment, so count from the scores), reserve that many slots of
+        // the sequence's candidate buffer with one atomic, then write them
         {
             uint32_t mine = 0;
-            for (int i = tid * (kHistBins / kThreads); i < (tid + 1) * (kHistBins / kThreads); ++i)
-                if (i >= T) mine += hist[i];
+            for (int i = tid; i < n; i += kThreads)
+                mine += static_cast<int>(key_bin(score_key(cscores[i]))) >= T ? 1u : 0u;
             for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
             if (lane == 0) ks->sel.scratch[warp] = mine;
             __syncthreads();
             if (tid == 0) {
                 uint32_t tot = 0;
                 for (int w8 = 0; w8 < kThreads / 32; ++w8) tot += ks->sel.scratch[w8];
-                ks->ncand = 0;
-                ks->ticket = atomicAdd(p.seqcnt + b, tot);   // base slot of this chunk
+                ks->sel.nsel = 0;
+                ks->ticket = tot ? atomicAdd(p.seqcnt + b, tot) : 0u;   // base slot of this CTA
             }
             __syncthreads();
         }
         uint64_t* cl = p.cand + static_cast<int64_t>(b) * p.cand_cap + ks->ticket;
-        const int nround = (n + kThreads - 1) / kThreads * kThreads;
         for (int i = tid; i < nround; i += kThreads) {
             uint32_t kk = 0;
             bool take = false;
@@ -510,10 +622,9 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
                 kk = score_key(cscores[i]);
                 take = static_cast<int>(key_bin(kk)) >= T;
             }
-            warp_append(cl, &ks->ncand, 0xFFFFFFFFu, make_comp(kk, key_begin + i), take);
+            warp_append(cl, &ks->sel.nsel, 0xFFFFFFFFu, make_comp(kk, key_begin + i), take);
+            hist_add_warp(gh, key_bin(kk), take);   // the published set's histogram
         }
-        for (int i = tid; i < kHistBins; i += kThreads)
-            if (i >= T && hist[i]) atomicAdd(gh + i, hist[i]);
         __threadfence();
         __syncthreads();
         if (tid == 0) {
@@ -524,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
         __syncthreads();
         if (ks->ticket != static_cast<uint32_t>(nch - 1)) return;
 
-        // ------------------------------------------------ sequence merge (last chunk)
+        // ------------------------------------------------ sequence merge (last CTA)
         __threadfence();
         copy_hist_global(hist, gh);
         const uint32_t flagged = __ldcg(p.seqflag + b);
@@ -538,12 +649,11 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
                 if (os) os[j] = -INFINITY;
             }
         } else {
-            uint64_t* sel = reinterpret_cast<uint64_t*>(a_tiles);
-            uint64_t* bndbuf = sel + IDX_MAX_TOPK;
-            const int bcap = (kStages * plan.a_stage_bytes - IDX_MAX_TOPK * 8) / 8;
+            uint64_t* buf = reinterpret_cast<uint64_t*>(a_tiles);
+            const int cap = kStages * plan.a_stage_bytes / 8;
             const uint64_t* L = p.cand + static_cast<int64_t>(b) * p.cand_cap;
             auto each = [&](auto f) { walk_global(L, total, f); };
-            select_topk_from_hist(each, hist, k, sel, bndbuf, bcap, &ks->sel, oi, os);
+            select_topk_from_hist<kDecodeSortE>(each, hist, k, buf, cap, &ks->sel, oi, os);
         }
         // leave the per-sequence state zeroed for the next call
         __syncthreads();

@@ -7,8 +7,8 @@
 // Long-Context Recall Failure" (section "Assumptions and Input Knowledge").
 //
 // One token per half-warp: each of the 16 lanes loads 16 bytes (8 bf16) of
-// the key.  fp8: the half-warp reduces amax with shuffles, divides (IEEE) by
-// the scale, converts pairs with the hardware e4m3 convert (round to nearest
+// the key.  fp8: the half-warp reduces amax with shuffles, divides by the
+// scale (correctly rounded, as IEEE division), converts pairs with the hardware e4m3 convert (round to nearest
 // even, saturating), pairs of lanes merge their 8 code bytes so that 8 lanes
 // write the 128-byte code row as 16-byte stores, and lane 0 writes the scale.
 // bf16: each lane copies its 16 bytes to the slot.
@@ -66,9 +66,10 @@ __global__ void __launch_bounds__(256) store_keys_kernel(const uint4* __restrict
             const float scale = __fdiv_rn(amax, 448.0f);
             uint32_t lo = 0, hi = 0;
             if (amax != 0.0f) {
+                const DivBy div(scale);
                 float y[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(x[i], scale);
+                for (int i = 0; i < 8; ++i) y[i] = div(x[i]);
                 lo = cvt_e4m3x2(y[0], y[1]) | (cvt_e4m3x2(y[2], y[3]) << 16);
                 hi = cvt_e4m3x2(y[4], y[5]) | (cvt_e4m3x2(y[6], y[7]) << 16);
             }

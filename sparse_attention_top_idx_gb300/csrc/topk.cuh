@@ -230,6 +230,87 @@ __device__ __forceinline__ void bitonic_sort_desc(uint64_t* a, int n) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Block sort, descending, of 256 * E composites held E per thread (thread t
+// owns positions t*E .. t*E+E-1).  Bitonic network: compare-exchanges between
+// a thread's own registers, then across lanes with warp shuffles, and through
+// shared memory (two block barriers a stage) only for strides that cross
+// warps: for 4096 keys, 6 of the 78 stages.
+// ---------------------------------------------------------------------------
+template <int E, int SIZE, int STRIDE>
+__device__ __forceinline__ void bsort_stage(uint64_t (&v)[E], uint64_t* a) {
+    const int t = threadIdx.x;
+    if constexpr (STRIDE >= 32 * E) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) a[t * E + e] = v[e];
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int i = t * E + e;
+            const uint64_t p = a[i ^ STRIDE];
+            const bool keep_max = ((i & STRIDE) == 0) == ((i & SIZE) == 0);
+            v[e] = keep_max ? (v[e] > p ? v[e] : p) : (v[e] < p ? v[e] : p);
+        }
+        __syncthreads();
+    } else if constexpr (STRIDE >= E) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int i = t * E + e;
+            const uint64_t p = __shfl_xor_sync(0xffffffffu, static_cast<unsigned long long>(v[e]), STRIDE / E);
+            const bool keep_max = ((i & STRIDE) == 0) == ((i & SIZE) == 0);
+            v[e] = keep_max ? (v[e] > p ? v[e] : p) : (v[e] < p ? v[e] : p);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            if ((e & STRIDE) == 0) {
+                const bool desc = ((t * E + e) & SIZE) == 0;
+                const uint64_t x = v[e], y = v[e + STRIDE];
+                if ((x < y) == desc) {
+                    v[e] = y;
+                    v[e + STRIDE] = x;
+                }
+            }
+        }
+    }
+}
+template <int E, int SIZE, int STRIDE>
+__device__ __forceinline__ void bsort_strides(uint64_t (&v)[E], uint64_t* a) {
+    bsort_stage<E, SIZE, STRIDE>(v, a);
+    if constexpr (STRIDE > 1) bsort_strides<E, SIZE, STRIDE / 2>(v, a);
+}
+template <int E, int SIZE>
+__device__ __forceinline__ void bsort_sizes(uint64_t (&v)[E], uint64_t* a) {
+    bsort_strides<E, SIZE, SIZE / 2>(v, a);
+    if constexpr (SIZE < kTopkThreads * E) bsort_sizes<E, SIZE * 2>(v, a);
+}
+// Sorts a[0 .. 256*E) in place (shared memory), descending.  All 256 threads.
+template <int E>
+__device__ __forceinline__ void block_sort_desc(uint64_t* a) {
+    uint64_t v[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = a[threadIdx.x * E + e];
+    bsort_sizes<E, 2>(v, a);
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < E; ++e) a[threadIdx.x * E + e] = v[e];
+    __syncthreads();
+}
+// Sorts a[0 .. n) descending for n <= 256 * kMaxE; entries up to the next
+// size step (256, 512, ...) are overwritten with zero padding.
+template <int kMaxE>
+__device__ __forceinline__ void block_sort_desc_n(uint64_t* a, int n) {
+    int n2 = kTopkThreads;
+    while (n2 < n) n2 <<= 1;
+    for (int i = n + static_cast<int>(threadIdx.x); i < n2; i += kTopkThreads) a[i] = 0ull;
+    __syncthreads();
+    if (n2 <= 256) block_sort_desc<1>(a);
+    else if (n2 <= 512) block_sort_desc<2>(a);
+    else if (n2 <= 1024) block_sort_desc<4>(a);
+    else if (kMaxE <= 8 || n2 <= 2048) block_sort_desc<(kMaxE < 8 ? kMaxE : 8)>(a);
+    else block_sort_desc<kMaxE>(a);
+}
+
 __device__ __forceinline__ int next_pow2(int x) {
     int p = 1;
     while (p < x) p <<= 1;
@@ -237,22 +318,48 @@ __device__ __forceinline__ int next_pow2(int x) {
 }
 
 // Final selection of one query row from a candidate set whose 4096-bin
-// histogram `hist` (shared) is exact.  `each` walks every candidate.  sel: shared buffer of >= next_pow2(k)
-// composites; bndbuf: shared buffer of bcap composites.  Writes the k outputs
-// (descending, -1 / -inf padded).  Called by all 256 threads.
-template <class Each>
-__device__ void select_topk_from_hist(Each each, const uint32_t* hist, int k, uint64_t* sel,
-                                      uint64_t* bndbuf, int bcap, SelectSmem* ss,
-                                      int32_t* out_idx, float* out_score) {
+// histogram `hist` (shared) is exact.  `each` walks every candidate.  buf:
+// shared buffer of cap >= 2048 + (boundary room) composites; up to 256 * kMaxE
+// candidates at or above the boundary bin are selected by one sort.  Writes the k outputs (descending,
+// -1 / -inf padded).  Called by all 256 threads.
+template <int kMaxE, class Each>
+__device__ void select_topk_from_hist(Each each, const uint32_t* hist, int k, uint64_t* buf, int cap,
+                                      SelectSmem* ss, int32_t* out_idx, float* out_score) {
     const int tid = threadIdx.x;
     block_find_suffix(hist, kHistBins, static_cast<uint32_t>(k), ss->scratch, &ss->bnd);
     const int bstar = ss->bnd.bin;
     const uint32_t above = ss->bnd.above;
+    const uint32_t count_ge = above + ss->bnd.at;     // candidates in bins >= bstar
     if (tid == 0) {
         ss->nsel = 0;
         ss->nbnd = 0;
     }
     __syncthreads();
+    const uint32_t sortcap = static_cast<uint32_t>(min(cap, kTopkThreads * kMaxE));
+    if (count_ge <= sortcap) {
+        // common case: everything at or above the boundary bin fits; one sort
+        each([&](uint64_t c, bool v) {
+            warp_append(buf, &ss->nsel, sortcap, c, v && static_cast<int>(comp_key(c) >> kHistShift) >= bstar);
+        });
+        __syncthreads();
+        block_sort_desc_n<kMaxE>(buf, static_cast<int>(count_ge));
+        const int nsel = min(k, static_cast<int>(count_ge));
+        for (int j = tid; j < k; j += kTopkThreads) {
+            if (j < nsel) {
+                const uint64_t c = buf[j];
+                out_idx[j] = comp_index(c);
+                if (out_score) out_score[j] = key_score(comp_key(c));
+            } else {
+                out_idx[j] = -1;
+                if (out_score) out_score[j] = -INFINITY;
+            }
+        }
+        return;
+    }
+    // many candidates share the boundary bin: refine it by radix passes
+    uint64_t* sel = buf;
+    uint64_t* bndbuf = buf + IDX_MAX_TOPK;
+    const int bcap = cap - IDX_MAX_TOPK;
     // gather: bins above the boundary go straight to sel, the boundary bin to bndbuf
     each([&](uint64_t c, bool v) {
         const int b = static_cast<int>(comp_key(c) >> kHistShift);
@@ -281,10 +388,7 @@ __device__ void select_topk_from_hist(Each each, const uint32_t* hist, int k, ui
         __syncthreads();
     }
     const int nsel = (bstar >= 0) ? k : static_cast<int>(above);
-    const int n2 = next_pow2(nsel < 1 ? 1 : nsel);
-    for (int i = nsel + tid; i < n2; i += kTopkThreads) sel[i] = 0ull;
-    __syncthreads();
-    bitonic_sort_desc(sel, n2);
+    block_sort_desc_n<8>(sel, nsel);
     for (int j = tid; j < k; j += kTopkThreads) {
         if (j < nsel) {
             uint64_t c = sel[j];

@@ -43,16 +43,20 @@ def test_store_bit_exact(bs, mode):
     assert diff.size == 0, "first differing byte %d of %d" % (diff[0], diff.size)
 
 
-def test_e4m3_convert_every_bf16_below_448():
-    # Rows whose largest magnitude is 448 have scale exactly 1, so the codes
-    # are the e4m3 encodings of the bf16 values themselves: every finite bf16
-    # magnitude up to 448, both signs, against the oracle's encoder.
-    pos = np.arange(0, 0x43E1, dtype=np.uint16)          # bf16 0 .. 448
+@pytest.mark.parametrize("amax", [448.0, 1344.0, 336.0, 1000.0])
+def test_e4m3_convert_every_bf16_below_amax(amax):
+    # Every finite bf16 magnitude up to amax, both signs, in rows whose
+    # largest magnitude is amax, against the oracle's encoder.  amax = 448
+    # gives scale exactly 1 (the codes are the e4m3 encodings of the bf16
+    # values themselves); 1344, 336 and 1000 give scales 3, 0.75 and 1000/448,
+    # where x / scale is inexact and its correct rounding decides ties.
+    top = int(wl.f32_to_bf16_bits(np.array([amax], np.float32))[0])
+    pos = np.arange(0, top + 1, dtype=np.uint16)
     vals = np.concatenate([pos, pos | 0x8000])
     per = 127
     nrows = (len(vals) + per - 1) // per
     rows = np.zeros((nrows, 128), np.uint16)
-    rows[:, 0] = 0x43E0                                    # 448.0
+    rows[:, 0] = top
     flat = np.zeros(nrows * per, np.uint16)
     flat[:len(vals)] = vals
     rows[:, 1:] = flat.reshape(nrows, per)
@@ -64,8 +68,10 @@ def test_e4m3_convert_every_bf16_below_448():
     got = cache.pool.cpu().numpy().reshape(nblk, 8448)
     codes = np.concatenate([got[b, :bs * 128].reshape(bs, 128) for b in range(nblk)])[:nrows]
     scales = np.concatenate([got[b, bs * 128:].view(np.float32) for b in range(nblk)])[:nrows]
-    assert np.all(scales == 1.0)
-    want, _ = oracle.quantize_rows(rows)
+    want, want_s = oracle.quantize_rows(rows)
+    assert np.array_equal(scales.view(np.uint32), want_s.view(np.uint32))
+    if amax == 448.0:
+        assert np.all(scales == 1.0)
     assert np.array_equal(codes, want)
 
 
