@@ -221,14 +221,37 @@ def capture(fn, steps, start, device, evs=None):
     return g
 
 
+EAGER = False   # --eager: issue the timed steps call by call (for profiler runs)
+
+
 def time_steps(bench, steps, warmup, dist, device):
     """W warm-up steps, then exactly K timed steps replayed from one CUDA graph
     between barriers and synchronisations; per-step events around the scoring
-    kernel give its launch durations."""
+    kernel give its launch durations.  With --eager the steps are issued call
+    by call instead (profiler runs)."""
     import torch
     for i in range(warmup):
         bench.step(i)
     torch.cuda.synchronize(device)
+    if EAGER:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        torch.cuda.synchronize(device)
+        t0.record()
+        for i in range(steps):
+            bench.step(warmup + i, evs[i])
+        t1.record()
+        torch.cuda.synchronize(device)
+        barrier(dist)
+
+        class _Replay:
+            def replay(self):
+                for i in range(steps):
+                    bench.step(warmup + i)
+        return t0.elapsed_time(t1), [a.elapsed_time(b) for a, b in evs], _Replay()
     evs = _timing_events(steps)
     g = capture(bench.step, steps, warmup, device, evs)
     g.replay()                                # untimed: first replay uploads the graph
@@ -456,11 +479,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the long-context and prefill objects")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    ap.add_argument("--eager", action="store_true", help="no CUDA graphs (for profiler runs)")
     ap.add_argument("--only", choices=["longctx", "prefill"], default=None,
                     help="run just one secondary workload and print its object (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    global EAGER
+    EAGER = args.eager
     if args.impl == "reference":
         return run_reference(args)
 

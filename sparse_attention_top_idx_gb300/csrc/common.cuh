@@ -204,6 +204,25 @@ __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void dsmem_st_u64(uint32_t addr, uint64_t v) {
     asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+// Asynchronous remote stores: the bytes are counted on an mbarrier of the
+// receiving CTA (complete_tx), which publishes them to its waiters; no fence
+// or arrive by the sender is needed.  addr and bar are shared::cluster
+// addresses in the same CTA.
+__device__ __forceinline__ void dsmem_st_async_v4(uint32_t addr, uint4 v, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+        "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void dsmem_st_async_u64(uint32_t addr, uint64_t v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(addr), "l"(v),
+                 "r"(bar)
+                 : "memory");
+}
+
 // Release-arrive on an mbarrier of any CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
@@ -331,6 +350,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------------------
+// packed fp32 pairs (two lanes of one 64-bit register)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long r) {
+    float x, y;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+    return make_float2(x, y);
+}
+// Two independent fp32 fused multiply-adds, each rounded to nearest even.
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
 }
 
 // ---------------------------------------------------------------------------

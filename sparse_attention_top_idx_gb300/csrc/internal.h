@@ -24,9 +24,11 @@ struct idx_cache {
 
 namespace dsaidx {
 
-constexpr int kThreads = 256;        // every kernel of the scoring path
+constexpr int kThreads = 256;        // decode scoring and selection kernels
+constexpr int kPrefillThreads = 384; // prefill scoring: 8 epilogue warps
 constexpr int kTileKeys = 128;       // keys per MMA tile (M)
 constexpr int kPrefillQT = 4;        // queries per prefill CTA (N = 64 * 4 = 256)
+constexpr int kBidWindow = 256;      // block ids the TMA producer warp prefetches at a time
 
 // Parameters of the scoring kernels (decode fused top-k, prefill scores).
 struct ScoreParams {
@@ -65,7 +67,7 @@ struct ScoreParams {
 // Shared-memory plan of the scoring kernel for (fp8, queries per CTA, chunk).
 struct SmemPlan {
     int stages, a_stage_bytes, q_bytes, n_cols;
-    int a_off, q_off, scale_off, w_off, hist_off, raw_off, misc_off, bar_off;
+    int a_off, q_off, scale_off, w_off, hist_off, raw_off, bid_off, misc_off, bar_off;
     int total;   // bytes to request (includes 1 KB of alignment slack)
 };
 
@@ -87,6 +89,7 @@ __host__ __device__ inline SmemPlan make_plan(bool fp8, int qt, int chunk) {
     p.w_off = o;       o += p.n_cols * 4;
     p.hist_off = o;    o += (qt == 1) ? 4096 * 4 : 0;
     p.raw_off = o;     o += raw_bytes;
+    p.bid_off = o;     o += kBidWindow * 4;  // prefetched block ids
     p.misc_off = o;    o += 4096;            // selection scratch, flags, group scan
     p.bar_off = o;     o += 256;             // mbarriers
     p.total = o + 1024;

@@ -79,7 +79,7 @@ cudaError_t launch_prefill_t(const idx_cache* c, const ScoreParams& p, cudaStrea
     cudaError_t e = set_smem_once(kern, plan.total, attr_done);
     if (e != cudaSuccess) return e;
     if (p.num_groups > 0) {
-        kern<<<p.num_groups, kThreads, plan.total, st>>>(c->tmap, p);
+        kern<<<p.num_groups, kPrefillThreads, plan.total, st>>>(c->tmap, p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -47,14 +47,15 @@ struct KernelShared {
     uint32_t ticket;
     int unit_b, key_begin, key_end, seq_len, nrows, row0, nq;
     int seg, nseg;      // decode: segment of the sequence and segments in it
-    int cl_bin;         // decode: boundary bin broadcast by the cluster leader
-    uint32_t cl_mode;   // decode: selection mode broadcast by the leader
+    uint64_t cl_word;   // decode: boundary bin (low 32 bits) and selection mode
+                        // (high 32 bits) broadcast by the cluster leader
     uint32_t cl_count;  // decode: candidates at or above the boundary (leader)
     uint32_t cl_flag;   // decode: a CTA of the segment failed a device check
     int pos[kPrefillQT];
     SelectSmem sel;
-    uint32_t grp[kThreads];   // prefill: group-count scan
+    uint32_t grp[kPrefillThreads];   // prefill: group-count scan
 };
+static_assert(sizeof(KernelShared) <= 4096, "KernelShared must fit the misc region");
 
 // e4m3 encode of two fp32 values (lo = a, hi = b) by the hardware convert.
 __device__ __forceinline__ uint32_t cvt_e4m3x2_pair(float a, float b) {
@@ -81,83 +82,117 @@ __device__ __forceinline__ void copy_hist_global(uint32_t* dst, const uint32_t* 
     for (int u = 0; u < 4; ++u) d4[u * 256 + threadIdx.x] = v[u];
 }
 
-// Quantise (fp8) or copy (bf16) the CTA's query rows, staged in shared memory
-// as raw [nrows][64][128] bf16 with their head weights in wq, into the B
-// operand tile, and turn wq into w'.  Row n = j * 64 + h (query j, head h);
-// rows of missing queries (j >= nrows) get zero codes and zero weight.  fp8:
-// per row scale sq = amax / 448 (IEEE), codes e4m3(q / sq) with the quotient
-// correctly rounded, w' = w * sq; amax = 0 gives zero codes and w' = 0 * w.
-// Four consecutive threads per row (32 elements each); t / nthreads: this
-// thread's index among the nthreads doing the work.
+// One quarter (32 elements, `part` 0..3) of query row r, staged in shared
+// memory as bf16, turned into its B-tile content.  fp8: per row scale
+// sq = amax / 448 (IEEE; the four lanes of gmask share the row and reduce
+// amax), codes e4m3(q / sq) with the quotient correctly rounded, returned as
+// two 16-byte chunks (row chunks 2 part and 2 part + 1), w' = w * sq; amax = 0
+// gives zero codes.  bf16: the 64 bytes as four chunks (B-tile half part / 2,
+// chunks 4 (part & 1) .. +3), w' = w.  A missing row (have = false) gives
+// zero chunks and w' = 0.
+template <bool kFp8>
+__device__ __forceinline__ float quant_row_part(const uint8_t* raw_row, int part, bool have, float wv,
+                                                unsigned gmask, uint4 (&out)[4]) {
+    uint4 v[4];
+    if (have) {
+        const uint4* src = reinterpret_cast<const uint4*>(raw_row + part * 64);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = src[i];
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = make_uint4(0, 0, 0, 0);
+        wv = 0.0f;
+    }
+    if constexpr (!kFp8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) out[i] = v[i];
+        return wv;
+    } else {
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[8 * i + 2 * e] = __uint_as_float(w4[e] << 16);
+                x[8 * i + 2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
+            }
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
+        const float sq = __fdiv_rn(amax, 448.0f);
+        const DivBy div(sq);
+        uint32_t c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (amax != 0.0f) {
+                const float y0 = div(x[4 * i + 0]), y1 = div(x[4 * i + 1]);
+                const float y2 = div(x[4 * i + 2]), y3 = div(x[4 * i + 3]);
+                c[i] = cvt_e4m3x2_pair(y0, y1) | (cvt_e4m3x2_pair(y2, y3) << 16);
+            } else {
+                c[i] = 0;
+            }
+        }
+        out[0] = make_uint4(c[0], c[1], c[2], c[3]);
+        out[1] = make_uint4(c[4], c[5], c[6], c[7]);
+        return wv * sq;
+    }
+}
+
+// Byte offset in the B tile of chunk i (0..3) produced by quant_row_part.
+template <bool kFp8>
+__device__ __forceinline__ int qchunk_off(int r, int part, int i, int rows) {
+    if constexpr (kFp8) return sw128_off(r, 2 * part + i);
+    else return (part >> 1) * (rows * 128) + sw128_off(r, (part & 1) * 4 + i);
+}
+
+// All query rows of a CTA (prefill), staged as raw [nrows][64][128] bf16 with
+// their head weights in wq: builds the B tile and turns wq into w'.  Row
+// n = j * 64 + h; rows of missing queries (j >= nrows) get zero codes and zero
+// weight.  Four consecutive threads per row; t / nthreads: this thread's index
+// among the nthreads doing the work.
 template <bool kFp8, int kQT>
 __device__ __forceinline__ void prep_queries(const uint8_t* raw, int nrows, uint8_t* qtile, float* wq,
                                              int t, int nthreads) {
     constexpr int kRows = 64 * kQT;
+    constexpr int kChunks = kFp8 ? 2 : 4;
     const int part = t & 3;
     const unsigned gmask = 0xFu << (threadIdx.x & 28);   // the 4 lanes sharing a row
     for (int r = t >> 2; r < kRows; r += nthreads / 4) {
-        const int j = r >> 6;
-        const bool have = j < nrows;
-        uint4 v[4];
-        if (have) {
-            const uint4* src = reinterpret_cast<const uint4*>(raw + static_cast<size_t>(r) * 256 + part * 64);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = src[i];
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = make_uint4(0, 0, 0, 0);
-        }
+        const bool have = (r >> 6) < nrows;
         const float wv = have ? wq[r] : 0.0f;
         __syncwarp(gmask);   // every lane of the row has read wq[r]
-        if constexpr (!kFp8) {
-            // elements [32 part, 32 part + 32) = 64 bytes: half part / 2, chunks
-            // 4 * (part & 1) .. +3 of that half
-            uint8_t* half = qtile + (part >> 1) * (kRows * 128);
+        uint4 out[4];
+        const float wn = quant_row_part<kFp8>(raw + static_cast<size_t>(r) * 256, part, have, wv, gmask, out);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<uint4*>(half + sw128_off(r, (part & 1) * 4 + i)) = v[i];
-            if (part == 0) wq[r] = wv;
-        } else {
-            float x[32];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    x[8 * i + 2 * e] = __uint_as_float(w4[e] << 16);
-                    x[8 * i + 2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
-                }
-            }
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
-            const float sq = __fdiv_rn(amax, 448.0f);
-            const DivBy div(sq);
-            uint32_t c[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (amax != 0.0f) {
-                    const float y0 = div(x[4 * i + 0]), y1 = div(x[4 * i + 1]);
-                    const float y2 = div(x[4 * i + 2]), y3 = div(x[4 * i + 3]);
-                    c[i] = cvt_e4m3x2_pair(y0, y1) | (cvt_e4m3x2_pair(y2, y3) << 16);
-                } else {
-                    c[i] = 0;
-                }
-            }
-            // bytes [32 part, 32 part + 32) = chunks 2 part and 2 part + 1
-            *reinterpret_cast<uint4*>(qtile + sw128_off(r, 2 * part)) = make_uint4(c[0], c[1], c[2], c[3]);
-            *reinterpret_cast<uint4*>(qtile + sw128_off(r, 2 * part + 1)) = make_uint4(c[4], c[5], c[6], c[7]);
-            if (part == 0) wq[r] = wv * sq;
-        }
+        for (int i = 0; i < kChunks; ++i)
+            *reinterpret_cast<uint4*>(qtile + qchunk_off<kFp8>(r, part, i, kRows)) = out[i];
+        if (part == 0) wq[r] = wn;
     }
 }
 
+// Two decode CTAs share an SM only at <= 124 registers per thread (measured
+// with the occupancy API on GB300: 126 already limits it to one), hence the
+// explicit cap for the decode instantiation.
+template <int kQT>
+struct RegCap {
+    static constexpr int value = (kQT == 1) ? 120 : 168;   // 168 * 384 threads fits one SM
+};
+template <int kQT>
+struct BlockDim {
+    static constexpr int value = (kQT == 1) ? kThreads : kPrefillThreads;
+};
+
 template <bool kFp8, int kBs, int kQT>
-__global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
+__global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQT>::value)
     score_kernel(const __grid_constant__ CUtensorMap tmap, const ScoreParams p) {
     constexpr bool kDecode = (kQT == 1);
+    constexpr int kBlock = BlockDim<kQT>::value;
+    constexpr int kEpiWarps = kDecode ? 4 : 8;             // two per TMEM lane quadrant for prefill
+    constexpr int kQPer = kQT / (kEpiWarps / 4);           // queries per epilogue warp
     constexpr int kN = 64 * kQT;
     constexpr int kBlocksPerTile = kTileKeys / kBs;
     constexpr int kKSteps = kFp8 ? 4 : 8;
@@ -188,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
     uint64_t* hbar = bars + 14;            // decode leader: every CTA's histogram added
     uint64_t* bbar = bars + 15;            // decode: boundary bin broadcast received
     uint64_t* gbar = bars + 16;            // decode leader: every CTA's candidates pushed
+    uint64_t* qready = bars + 17;          // decode: every rank's query rows written here
 
     const int tid = threadIdx.x;
     const int warp = warp_id(), lane = lane_id();
@@ -234,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
         // group g of up to 4 rows of one sequence; longest rows first
         const int g = gridDim.x - 1 - blockIdx.x;
         uint32_t mine = 0;
-        const int per = (p.batch + kThreads - 1) / kThreads;
+        const int per = (p.batch + kBlock - 1) / kBlock;
         for (int i = 0; i < per; ++i) {
             const int bb = tid * per + i;
             if (bb < p.batch) {
@@ -246,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
         __syncthreads();
         if (tid == 0) {
             uint32_t acc = 0;
-            for (int i = 0; i < kThreads; ++i) {
+            for (int i = 0; i < kBlock; ++i) {
                 const uint32_t v = ks->grp[i];
                 ks->grp[i] = acc;   // exclusive prefix
                 acc += v;
@@ -299,20 +335,27 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kFp8 ? 1 + 4 : 1);
+            mbar_init(&empty[s], kFp8 ? 1 + kEpiWarps : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 4);
+            mbar_init(&tempty[a], kEpiWarps);
         }
         mbar_init(mdone, 1);
         mbar_init(qbar, 1);
         if constexpr (kDecode) {
-            mbar_init(hbar, p.cluster * kThreads);
+            mbar_init(hbar, p.cluster);
+            // bbar and qready complete when their bytes have arrived (st.async);
+            // gbar when the leader has announced the byte count and it arrived
             mbar_init(bbar, 1);
-            mbar_init(gbar, p.cluster * kThreads);
+            mbar_init(gbar, 1);
+            mbar_init(qready, 1);
         }
         fence_mbar_init();
+        if constexpr (kDecode) {
+            mbar_arrive_expect_tx(bbar, 8);
+            mbar_arrive_expect_tx(qready, 64 * (kFp8 ? 128 : 256) + 64 * 4);
+        }
         ks->abort = 0;
         ks->bad = 0;
         ks->ncand = 0;
@@ -333,75 +376,146 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
     if constexpr (kDecode) cluster_sync_all();
     const uint32_t tmem = ks->tmem_base;
 
-    // Warp 0 stages the query rows and starts streaming keys at once; warps
-    // 1..7 build the query tile meanwhile and meet on a named barrier before
-    // the first MMA.
-    if (warp != 0) {
+    // Warp 0 stages the query rows and starts streaming keys at once.  Decode:
+    // each rank of the cluster quantises 64 / cluster of the 64 head rows
+    // (warp 2) and warps 1..7 send them, as one contiguous run of the 128-byte
+    // swizzled B tile (row r is bytes [128 r, 128 r + 128)) plus the rows'
+    // weights, to every rank as st.async counted on that rank's qready.
+    // Prefill: warps 1..11 build the whole tile and meet on a named barrier.
+    int qrow0 = 0, qrows = 0;
+    if constexpr (kDecode) {
+        qrows = 64 / p.cluster;
+        qrow0 = static_cast<int>(cluster_rank()) * qrows;
+        constexpr int kChunks = kFp8 ? 2 : 4;
+        const int i = tid - 64;
+        if (i >= 0 && i < qrows * 4) {
+            const int r = qrow0 + (i >> 2), part = i & 3;
+            const unsigned gmask = 0xFu << (threadIdx.x & 28);
+            if (!mbar_wait(qbar, 0, status, &ks->abort)) ks->abort = 1;
+            const float wv = wq[r];
+            uint4 out[4];
+            const float wn = quant_row_part<kFp8>(raw + static_cast<size_t>(r) * 256, part, true, wv, gmask, out);
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+                *reinterpret_cast<uint4*>(qtile + qchunk_off<kFp8>(r, part, c, 64)) = out[c];
+            if (part == 0) wq[r] = wn;
+        }
+        if (warp != 0) {
+            asm volatile("bar.sync 2, %0;" ::"r"(kThreads - 32) : "memory");
+            const int run = qrows * 128 / 16;                  // 16-byte chunks per half
+            const int per_rank = run * (kFp8 ? 1 : 2) + qrows * 4 / 16;
+            for (int j = tid - 32; j < per_rank * p.cluster; j += kThreads - 32) {
+                const int rk = j / per_rank, c = j - rk * per_rank;
+                const uint32_t qb = dsmem_addr(qready, static_cast<uint32_t>(rk));
+                const uint8_t* src;
+                if (c < run * (kFp8 ? 1 : 2)) {
+                    const int half = c / run, cc = c - half * run;
+                    src = qtile + half * (64 * 128) + qrow0 * 128 + cc * 16;
+                } else {
+                    src = reinterpret_cast<const uint8_t*>(wq + qrow0) + (c - run * (kFp8 ? 1 : 2)) * 16;
+                }
+                dsmem_st_async_v4(dsmem_addr(src, static_cast<uint32_t>(rk)), *reinterpret_cast<const uint4*>(src), qb);
+            }
+        }
+    } else if (warp != 0) {
         if (!__all_sync(0xffffffffu, mbar_wait(qbar, 0, status, &ks->abort))) ks->abort = 1;
-        prep_queries<kFp8, kQT>(raw, ks->nrows, qtile, wq, tid - 32, kThreads - 32);
+        prep_queries<kFp8, kQT>(raw, ks->nrows, qtile, wq, tid - 32, kBlock - 32);
         fence_proxy_async_smem();
-        asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"r"(kBlock - 32) : "memory");
     }
 
     // ------------------------------------------------------------ main loop
-    if (warp == 0 && lane == 0) {
-        // query rows (bf16) and their head weights, one bulk copy each
-        const uint64_t pol_q = policy_evict_first();
-        const int nrows = ks->nrows;
-        mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(nrows) * (64 * kHeadDim * 2 + 64 * 4));
-        bulk_load(raw, p.q + static_cast<int64_t>(ks->row0) * 64 * kHeadDim,
-                  static_cast<uint32_t>(nrows) * 64 * kHeadDim * 2, qbar, pol_q);
-        bulk_load(wq, p.w + static_cast<int64_t>(ks->row0) * 64, static_cast<uint32_t>(nrows) * 64 * 4, qbar, pol_q);
-        // TMA producer of the key tiles
+    if (warp == 0) {
+        // Warp 0: lane 0 stages the query rows and issues the key TMA; the
+        // whole warp prefetches the block ids of up to kBidWindow blocks at a
+        // time into shared memory, so no tile waits on a block-table load.
+        int* bids = reinterpret_cast<int*>(smem + plan.bid_off);
+        if (lane == 0) {
+            const uint64_t pol_q = policy_evict_first();
+            // decode: this rank's share of the 64 head rows; prefill: every row
+            const int r0 = kDecode ? qrow0 : 0;
+            const int nr = kDecode ? qrows : ks->nrows * 64;
+            const int64_t g0 = static_cast<int64_t>(ks->row0) * 64 + r0;
+            mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(nr) * (kHeadDim * 2 + 4));
+            bulk_load(raw + static_cast<size_t>(r0) * kHeadDim * 2, p.q + g0 * kHeadDim,
+                      static_cast<uint32_t>(nr) * kHeadDim * 2, qbar, pol_q);
+            bulk_load(wq + r0, p.w + g0, static_cast<uint32_t>(nr) * 4, qbar, pol_q);
+            tma_prefetch_desc(&tmap);
+        }
         const uint64_t pol = kDecode ? policy_evict_first() : policy_evict_last();
-        tma_prefetch_desc(&tmap);
+        const int lb_end = (key_end + kBs - 1) / kBs;
+        int lb_lo = 0, lb_hi = 0;          // window of prefetched logical blocks
         int t = 0;
         for (; t < ntiles; ++t) {
             const int s = t % kStages;
             const uint32_t ph = static_cast<uint32_t>(t / kStages) & 1u;
-            if (t >= kStages && !mbar_wait(&empty[s], ph ^ 1u, status, &ks->abort)) break;
             const int key0 = key_begin + t * kTileKeys;
-            int phys[kBlocksPerTile];
-            uint32_t bytes = 0;
+            const int lb0 = key0 / kBs;
+            if (lb0 + kBlocksPerTile > lb_hi && lb_hi < lb_end) {
+                __syncwarp();
+                lb_lo = lb0;
+                lb_hi = min(lb_end, lb0 + kBidWindow);
+                for (int i = lane; i < lb_hi - lb_lo; i += 32) {
+                    const int lb = lb_lo + i;
+                    bids[i] = (lb < p.mbps) ? p.block_table[static_cast<int64_t>(seq_b) * p.mbps + lb] : -1;
+                }
+                __syncwarp();
+            }
+            bool ok = true;
+            if (lane == 0) {
+                if (t >= kStages) ok = mbar_wait(&empty[s], ph ^ 1u, status, &ks->abort);
+                if (ok) {
+                    int phys[kBlocksPerTile];
+                    uint32_t bytes = 0;
 #pragma unroll
-            for (int j = 0; j < kBlocksPerTile; ++j) {
-                const int lb = key0 / kBs + j;
-                phys[j] = -1;
-                if (lb * kBs < key_end) {
-                    const int pb = (lb < p.mbps) ? p.block_table[static_cast<int64_t>(seq_b) * p.mbps + lb] : -1;
-                    if (pb < 0 || pb >= p.num_blocks) {
-                        ks->bad = 1;
-                        set_status(status, IDX_ERR_DEVICE_CHECK);
-                    } else {
-                        phys[j] = pb;
-                        bytes += kBlockTx;
+                    for (int j = 0; j < kBlocksPerTile; ++j) {
+                        const int lb = lb0 + j;
+                        phys[j] = -1;
+                        if (lb * kBs < key_end) {
+                            const int pb = bids[lb - lb_lo];
+                            if (pb < 0 || pb >= p.num_blocks) {
+                                ks->bad = 1;
+                                set_status(status, IDX_ERR_DEVICE_CHECK);
+                            } else {
+                                phys[j] = pb;
+                                bytes += kBlockTx;
+                            }
+                        }
+                    }
+                    uint8_t* a_s = a_tiles + s * plan.a_stage_bytes;
+                    mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+                    for (int j = 0; j < kBlocksPerTile; ++j) {
+                        if (phys[j] < 0) continue;
+                        if constexpr (kFp8) {
+                            tma_load_3d(a_s + j * kBs * 128, &tmap, &full[s], 0, 0, phys[j], pol);
+                            bulk_load(scales + s * 128 + j * kBs,
+                                      p.pool + static_cast<int64_t>(phys[j]) * p.block_bytes + kBs * 128,
+                                      kBs * 4, &full[s], pol);
+                        } else {
+                            tma_load_3d(a_s + j * kBs * 128, &tmap, &full[s], 0, 0, phys[j], pol);
+                            tma_load_3d(a_s + 16384 + j * kBs * 128, &tmap, &full[s], 64, 0, phys[j], pol);
+                        }
                     }
                 }
             }
-            uint8_t* a_s = a_tiles + s * plan.a_stage_bytes;
-            mbar_arrive_expect_tx(&full[s], bytes);
-#pragma unroll
-            for (int j = 0; j < kBlocksPerTile; ++j) {
-                if (phys[j] < 0) continue;
-                if constexpr (kFp8) {
-                    tma_load_3d(a_s + j * kBs * 128, &tmap, &full[s], 0, 0, phys[j], pol);
-                    bulk_load(scales + s * 128 + j * kBs,
-                              p.pool + static_cast<int64_t>(phys[j]) * p.block_bytes + kBs * 128,
-                              kBs * 4, &full[s], pol);
-                } else {
-                    tma_load_3d(a_s + j * kBs * 128, &tmap, &full[s], 0, 0, phys[j], pol);
-                    tma_load_3d(a_s + 16384 + j * kBs * 128, &tmap, &full[s], 64, 0, phys[j], pol);
-                }
-            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         }
-        // copies still in flight (only when a wait gave up) must land before exit
-        for (int u = max(0, t - kStages); u < t; ++u)
-            mbar_wait(&full[u % kStages], static_cast<uint32_t>(u / kStages) & 1u, status, nullptr);
-        mbar_wait(qbar, 0, status, nullptr);
+        if (lane == 0) {
+            // copies still in flight (only when a wait gave up) must land before exit
+            for (int u = max(0, t - kStages); u < t; ++u)
+                mbar_wait(&full[u % kStages], static_cast<uint32_t>(u / kStages) & 1u, status, nullptr);
+            mbar_wait(qbar, 0, status, nullptr);
+        }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer
         constexpr uint32_t idesc = idesc_make(kFp8, kTileKeys, kN);
         const uint32_t q_base = smem_u32(qtile);
+        if constexpr (kDecode) {
+            // the B tile was written by the cluster's ranks
+            if (!mbar_wait_cluster(qready, 0, status)) ks->abort = 1;
+            fence_proxy_async_smem();
+        }
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % kStages;
             const uint32_t ph = static_cast<uint32_t>(t / kStages) & 1u;
@@ -434,10 +548,15 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
         mma_commit(mdone);
         mbar_wait(mdone, 0, status, nullptr);
     } else if (warp >= 4) {
-        // epilogue: one key row per thread
+        // epilogue: one key row per thread; warp w reads TMEM lane quadrant
+        // w % 4 and queries j0 .. j0 + kQPer - 1 of the tile
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
+        const int j0 = ((warp - 4) >> 2) * kQPer;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(qd * 32) << 16);
+        if constexpr (kDecode) {
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(qready, 0, status))) ks->abort = 1;   // w'
+        }
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % kStages;
             const uint32_t ph = static_cast<uint32_t>(t / kStages) & 1u;
@@ -453,18 +572,24 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
-            float res[kQT];
+            // sum_h w'[h] * max(D[h], 0): even and odd heads in the two lanes of
+            // a packed fp32 pair, added at the end
+            float res[kQPer];
 #pragma unroll
-            for (int j = 0; j < kQT; ++j) {
-                float acc = 0.0f;
+            for (int jj = 0; jj < kQPer; ++jj) {
+                const int j = j0 + jj;
+                unsigned long long acc = 0ull;
+                const unsigned long long* w2 = reinterpret_cast<const unsigned long long*>(wq + j * 64);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     float v[32];
                     tmem_ld32(lane_base + static_cast<uint32_t>(a * kN + j * 64 + hh * 32), v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc = fmaf(wq[j * 64 + hh * 32 + i], fmaxf(v[i], 0.0f), acc);
+                    for (int i = 0; i < 16; ++i)
+                        acc = f2_fma(w2[hh * 16 + i], f2_pack(fmaxf(v[2 * i], 0.0f), fmaxf(v[2 * i + 1], 0.0f)), acc);
                 }
-                res[j] = kscale * acc;
+                const float2 pr = f2_unpack(acc);
+                res[jj] = kscale * (pr.x + pr.y);
             }
             tc_fence_before();
             __syncwarp();
@@ -477,9 +602,10 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
                 hist_add_warp(hist, key_bin(kk), valid);
             } else {
 #pragma unroll
-                for (int j = 0; j < kQT; ++j) {
+                for (int jj = 0; jj < kQPer; ++jj) {
+                    const int j = j0 + jj;
                     if (j < ks->nrows && key <= ks->pos[j])
-                        p.scores[static_cast<int64_t>(ks->row0 + j) * p.score_stride + key] = res[j];
+                        p.scores[static_cast<int64_t>(ks->row0 + j) * p.score_stride + key] = res[jj];
                 }
             }
         }
@@ -516,29 +642,55 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
             }
         }
         if (tid == 0 && (ks->bad || ks->abort)) dsmem_red_add(dsmem_addr(&ks->cl_flag, 0), 1u);
-        mbar_arrive_remote(dsmem_addr(hbar, 0));
+        // one release per CTA: the barrier orders every thread's remote adds
+        // before thread 0's cluster-scope fence and arrive
+        __syncthreads();
+        if (tid == 0) {
+            fence_acq_rel_cluster();
+            mbar_arrive_remote(dsmem_addr(hbar, 0));
+        }
         if (rank == 0) {
             if (!mbar_wait_cluster(hbar, 0, status)) ks->abort = 1;
             block_find_suffix(hist, kHistBins, static_cast<uint32_t>(k), ks->sel.scratch, &ks->sel.bnd);
+            const uint32_t count_ge = ks->sel.bnd.above + ks->sel.bnd.at;
+            const uint32_t mode = (ks->nseg == 1 && count_ge <= kDecodeSortCap) ? kModeSmem : kModeGlobal;
             if (tid == 0) {
-                const uint32_t count_ge = ks->sel.bnd.above + ks->sel.bnd.at;
-                const uint32_t mode = (ks->nseg == 1 && count_ge <= kDecodeSortCap) ? kModeSmem : kModeGlobal;
                 ks->cl_count = count_ge;
-                for (int r = 0; r < CL; ++r) {
-                    dsmem_st_u32(dsmem_addr(&ks->cl_bin, static_cast<uint32_t>(r)), static_cast<uint32_t>(ks->sel.bnd.bin));
-                    dsmem_st_u32(dsmem_addr(&ks->cl_mode, static_cast<uint32_t>(r)), mode);
-                    mbar_arrive_remote(dsmem_addr(bbar, static_cast<uint32_t>(r)));
-                }
+                // the pushed candidates complete gbar: announce their bytes
+                // before any CTA can learn the boundary
+                if (mode == kModeSmem) mbar_arrive_expect_tx(gbar, count_ge * 8u);
+            }
+            __syncthreads();
+            if (tid < CL) {
+                const uint64_t word = (static_cast<uint64_t>(mode) << 32) | static_cast<uint32_t>(ks->sel.bnd.bin);
+                dsmem_st_async_u64(dsmem_addr(&ks->cl_word, static_cast<uint32_t>(tid)), word,
+                                   dsmem_addr(bbar, static_cast<uint32_t>(tid)));
             }
         }
         if (!mbar_wait_cluster(bbar, 0, status)) ks->abort = 1;
-        const int bstar = ks->cl_bin;            // -1: fewer than k keys in the segment
-        const uint32_t mode = ks->cl_mode;
+        const int bstar = static_cast<int>(static_cast<uint32_t>(ks->cl_word));   // -1: fewer than k keys
+        const uint32_t mode = static_cast<uint32_t>(ks->cl_word >> 32);
         const int nround = (n + kThreads - 1) / kThreads * kThreads;
 
         if (mode == kModeSmem) {
-            const uint32_t lbuf = dsmem_addr(a_tiles, 0);
-            const uint32_t lcnt = dsmem_addr(&ks->ncand, 0);
+            // count this CTA's keys at or above the boundary, reserve that many
+            // slots of the leader's buffer with one remote atomic, and push them
+            // as st.async counted on the leader's gbar
+            uint32_t mine = 0;
+            for (int i = tid; i < n; i += kThreads)
+                mine += static_cast<int>(key_bin(score_key(cscores[i]))) >= bstar ? 1u : 0u;
+            for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+            if (lane == 0) ks->sel.scratch[warp] = mine;
+            __syncthreads();
+            if (tid == 0) {
+                uint32_t tot = 0;
+                for (int w8 = 0; w8 < kThreads / 32; ++w8) tot += ks->sel.scratch[w8];
+                ks->sel.nsel = 0;
+                ks->ticket = tot ? dsmem_atom_add(dsmem_addr(&ks->ncand, 0), tot) : 0u;
+            }
+            __syncthreads();
+            const uint32_t lbuf = dsmem_addr(a_tiles, 0) + 8u * ks->ticket;
+            const uint32_t lgbar = dsmem_addr(gbar, 0);
             for (int i = tid; i < nround; i += kThreads) {
                 uint32_t kk = 0;
                 bool take = false;
@@ -550,16 +702,15 @@ __global__ void __launch_bounds__(kThreads, (kQT == 1) ? 2 : 1)
                 if (m) {
                     const int leader = __ffs(m) - 1;
                     uint32_t base = 0;
-                    if (lane == leader) base = dsmem_atom_add(lcnt, static_cast<uint32_t>(__popc(m)));
+                    if (lane == leader) base = atomicAdd(&ks->sel.nsel, static_cast<uint32_t>(__popc(m)));
                     base = __shfl_sync(0xffffffffu, base, leader);
                     if (take) {
                         const uint32_t pos = base + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
-                        if (pos < kDecodeSortCap)
-                            dsmem_st_u64(lbuf + 8u * pos, make_comp(kk, key_begin + i));
+                        if (ks->ticket + pos < kDecodeSortCap)
+                            dsmem_st_async_u64(lbuf + 8u * pos, make_comp(kk, key_begin + i), lgbar);
                     }
                 }
             }
-            mbar_arrive_remote(dsmem_addr(gbar, 0));
             if (rank != 0) return;   // nothing touches this CTA's shared memory any more
             if (!mbar_wait_cluster(gbar, 0, status)) ks->abort = 1;
             __syncthreads();
