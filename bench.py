@@ -43,7 +43,12 @@ N_POOL_COPIES = 9
 # DRAM bytes per launch of the dominant kernels from ncu captures
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources they were taken on; a stale hash reports null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/score_kernel_decode_b32_s4500_10000_top512.md
+    ("decode", "cecde544ac6be281"): 31553280,
+    # profiles/score_kernel_prefill_s22000_t8192_top1024.md (scoring kernel)
+    ("prefill", "cecde544ac6be281"): 139460096 + 528051456,
+}
 
 
 def kernel_source_hash() -> str:
