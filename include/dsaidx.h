@@ -168,6 +168,36 @@ idx_status idx_score_topk_decode(const idx_cache* cache, const void* q_bf16_dev,
                                  int32_t* out_idx_dev, float* out_score_dev,
                                  void* workspace_dev, size_t ws_bytes, void* stream);
 
+/*
+ * Decode without a workspace argument, for callers that cannot allocate
+ * device memory: for example a plug-in that runs inside another framework's
+ * process, where device memory belongs to that framework's allocator, or a
+ * caller on a path where cudaMalloc / cudaFree are not allowed because they
+ * may synchronise the device.  (The pages have no counterpart: this is a
+ * convenience of this library.)
+ *
+ * Same arguments, results and errors as idx_score_topk_decode, without
+ * workspace_dev / ws_bytes.  The scratch lives in a fixed 8 MiB area of
+ * library-owned device memory that every GPU loading the library holds until
+ * the process exits; a shape whose idx_workspace_bytes_decode() exceeds
+ * 8 MiB (roughly batch * (16 KiB + 8 bytes * max_seq_len)) is rejected with
+ * IDX_ERR_WORKSPACE_TOO_SMALL before anything runs.  The call allocates
+ * nothing; it clears the part of the area it uses (an asynchronous memset on
+ * `stream`) and launches the decode kernel.
+ *  - The first call on each device looks up the area's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls share the area: calls that may overlap on the GPU (different
+ *    streams without ordering, or several host threads) race and corrupt each
+ *    other's results; issue them in one stream or order them explicitly.
+ *  - Device-side checks still produce -1 rows, but their status word is not
+ *    readable by the caller (use idx_score_topk_decode to read it).
+ */
+idx_status idx_score_topk_decode_static(const idx_cache* cache, const void* q_bf16_dev,
+                                        const float* w_dev, const int32_t* block_table_dev,
+                                        int max_blocks_per_seq, const int32_t* seq_lens_dev,
+                                        int batch, int max_seq_len, int heads, int topk,
+                                        int32_t* out_idx_dev, float* out_score_dev, void* stream);
+
 /* Workspace bytes a prefill call needs.  0 on invalid arguments. */
 size_t idx_workspace_bytes_prefill(const idx_cache* cache, int batch, int total_q,
                                    int max_seq_len, int heads, int topk);

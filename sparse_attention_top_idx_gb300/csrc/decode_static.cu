@@ -1,0 +1,66 @@
+// decode_static.cu -- the decode score + top-k call for callers that cannot
+// allocate device memory.  Its scratch (per-sequence tickets, histograms,
+// flags and the candidate buffer that idx_score_topk_decode keeps in the
+// caller's workspace) lives in a fixed array in the library's own device
+// memory instead, so the caller passes only inputs and outputs.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "dsaidx.h"
+#include "internal.h"
+
+namespace {
+
+// Largest scratch a call may need; every GPU that loads the library holds this
+// much device memory until the process exits.
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(8) << 20;   // 8 MiB
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+// Device address of g_decode_scratch, per device.  In host code the array's
+// name is only a host-side stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+std::mutex g_scratch_mu;
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+
+idx_status scratch_of_current_device(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return IDX_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return IDX_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return IDX_OK;
+}
+
+}  // namespace
+
+extern "C" idx_status idx_score_topk_decode_static(const idx_cache* cache, const void* q_bf16_dev,
+                                                   const float* w_dev, const int32_t* block_table_dev,
+                                                   int max_blocks_per_seq, const int32_t* seq_lens_dev,
+                                                   int batch, int max_seq_len, int heads, int topk,
+                                                   int32_t* out_idx_dev, float* out_score_dev, void* stream) {
+    if (!cache) return IDX_ERR_INVALID_ARG;
+    const size_t need = idx_workspace_bytes_decode(cache, batch, max_seq_len, heads, topk);
+    if (need == 0)   // invalid or unsupported shape: the regular call reports which
+        return idx_score_topk_decode(cache, q_bf16_dev, w_dev, block_table_dev, max_blocks_per_seq,
+                                     seq_lens_dev, batch, max_seq_len, heads, topk, out_idx_dev,
+                                     out_score_dev, nullptr, 0, stream);
+    if (need > kStaticScratchBytes) return IDX_ERR_WORKSPACE_TOO_SMALL;
+    void* scratch = nullptr;
+    const idx_status s = scratch_of_current_device(&scratch);
+    if (s != IDX_OK) return s;
+    // The scratch keeps whatever the previous call left; the counters,
+    // histograms and status word must start at zero, so clear the part used.
+    if (cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return IDX_ERR_CUDA;
+    return idx_score_topk_decode(cache, q_bf16_dev, w_dev, block_table_dev, max_blocks_per_seq, seq_lens_dev,
+                                 batch, max_seq_len, heads, topk, out_idx_dev, out_score_dev, scratch, need,
+                                 stream);
+}

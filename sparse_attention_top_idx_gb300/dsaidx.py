@@ -60,6 +60,8 @@ def load(path: Optional[str] = None):
     L.idx_workspace_init.restype = I
     L.idx_score_topk_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, P, P, P, SZ, P]
     L.idx_score_topk_decode.restype = I
+    L.idx_score_topk_decode_static.argtypes = [P, P, P, P, I, P, I, I, I, I, P, P, P]
+    L.idx_score_topk_decode_static.restype = I
     L.idx_workspace_bytes_prefill.argtypes = [P, I, I, I, I, I]
     L.idx_workspace_bytes_prefill.restype = SZ
     L.idx_score_topk_prefill.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, SZ, P]
@@ -164,6 +166,27 @@ def store_keys(cache: IndexCache, k_bf16: torch.Tensor, slot_mapping: torch.Tens
 
 def workspace_bytes_decode(cache: IndexCache, batch: int, max_seq_len: int, heads: int, topk: int) -> int:
     return int(load().idx_workspace_bytes_decode(cache.handle, batch, max_seq_len, heads, topk))
+
+
+def score_topk_decode_static(cache: IndexCache, q: torch.Tensor, w: torch.Tensor, block_table: torch.Tensor,
+                             seq_lens: torch.Tensor, max_seq_len: int, topk: int, out_idx: torch.Tensor,
+                             out_score: Optional[torch.Tensor] = None, stream=None):
+    """idx_score_topk_decode_static: decode without a workspace (the library's
+    own fixed 8 MiB scratch per GPU; calls must not overlap on the GPU)."""
+    B, H = q.shape[0], q.shape[1]
+    _need(q, torch.bfloat16, "q", (B, H, HEAD_DIM))
+    _need(w, torch.float32, "w", (B, H))
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens", (B,))
+    _need(out_idx, torch.int32, "out_idx", (B, topk))
+    if out_score is not None:
+        _need(out_score, torch.float32, "out_score", (B, topk))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch, max_blocks_per_seq]")
+    _check(load().idx_score_topk_decode_static(cache.handle, _ptr(q), _ptr(w), _ptr(block_table),
+                                               block_table.shape[1], _ptr(seq_lens), B, max_seq_len, H, topk,
+                                               _ptr(out_idx), _ptr(out_score), _stream(stream)),
+           "idx_score_topk_decode_static")
 
 
 def workspace_bytes_prefill(cache: IndexCache, batch: int, total_q: int, max_seq_len: int, heads: int,

@@ -16,7 +16,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = dsaidx.header_functions()
-    assert len(names) == 11, names
+    assert len(names) == 12, names
     for n in names:
         assert hasattr(lib, n), n
 
