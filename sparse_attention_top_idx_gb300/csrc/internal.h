@@ -25,7 +25,7 @@ struct idx_cache {
 namespace dsaidx {
 
 constexpr int kThreads = 256;        // decode scoring and selection kernels
-constexpr int kPrefillThreads = 384; // prefill scoring: 8 epilogue warps
+constexpr int kPrefillThreads = 640; // prefill scoring: 16 epilogue warps
 constexpr int kTileKeys = 128;       // keys per MMA tile (M)
 constexpr int kPrefillQT = 4;        // queries per prefill CTA (N = 64 * 4 = 256)
 constexpr int kBidWindow = 256;      // block ids the TMA producer warp prefetches at a time

@@ -53,7 +53,7 @@ struct KernelShared {
     uint32_t cl_flag;   // decode: a CTA of the segment failed a device check
     int pos[kPrefillQT];
     SelectSmem sel;
-    uint32_t grp[kPrefillThreads];   // prefill: group-count scan
+    uint32_t grp[kThreads];   // prefill: group-count scan (first 256 threads)
 };
 static_assert(sizeof(KernelShared) <= 4096, "KernelShared must fit the misc region");
 
@@ -179,7 +179,7 @@ __device__ __forceinline__ void prep_queries(const uint8_t* raw, int nrows, uint
 // explicit cap for the decode instantiation.
 template <int kQT>
 struct RegCap {
-    static constexpr int value = (kQT == 1) ? 120 : 168;   // 168 * 384 threads fits one SM
+    static constexpr int value = (kQT == 1) ? 120 : 96;    // 96 * 640 threads fits one SM
 };
 template <int kQT>
 struct BlockDim {
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
     score_kernel(const __grid_constant__ CUtensorMap tmap, const ScoreParams p) {
     constexpr bool kDecode = (kQT == 1);
     constexpr int kBlock = BlockDim<kQT>::value;
-    constexpr int kEpiWarps = kDecode ? 4 : 8;             // two per TMEM lane quadrant for prefill
+    constexpr int kEpiWarps = kDecode ? 4 : 16;            // one per (TMEM lane quadrant, query)
     constexpr int kQPer = kQT / (kEpiWarps / 4);           // queries per epilogue warp
     constexpr int kN = 64 * kQT;
     constexpr int kBlocksPerTile = kTileKeys / kBs;
@@ -270,19 +270,19 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
         // group g of up to 4 rows of one sequence; longest rows first
         const int g = gridDim.x - 1 - blockIdx.x;
         uint32_t mine = 0;
-        const int per = (p.batch + kBlock - 1) / kBlock;
-        for (int i = 0; i < per; ++i) {
+        const int per = (p.batch + kThreads - 1) / kThreads;   // the first 256 threads scan
+        for (int i = 0; i < per && tid < kThreads; ++i) {
             const int bb = tid * per + i;
             if (bb < p.batch) {
                 const int nq = p.cu_q[bb + 1] - p.cu_q[bb];
                 mine += static_cast<uint32_t>((max(nq, 0) + kQT - 1) / kQT);
             }
         }
-        ks->grp[tid] = mine;
+        if (tid < kThreads) ks->grp[tid] = mine;
         __syncthreads();
         if (tid == 0) {
             uint32_t acc = 0;
-            for (int i = 0; i < kBlock; ++i) {
+            for (int i = 0; i < kThreads; ++i) {
                 const uint32_t v = ks->grp[i];
                 ks->grp[i] = acc;   // exclusive prefix
                 acc += v;
@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
         if (ks->unit_b == -1) return;
         {
             // the thread whose range holds g finds the sequence
-            const uint32_t lo = ks->grp[tid];
-            if (mine > 0 && static_cast<uint32_t>(g) >= lo && static_cast<uint32_t>(g) < lo + mine) {
+            const uint32_t lo = tid < kThreads ? ks->grp[tid] : 0u;
+            if (tid < kThreads && mine > 0 && static_cast<uint32_t>(g) >= lo && static_cast<uint32_t>(g) < lo + mine) {
                 uint32_t acc = lo;
                 for (int i = 0; i < per; ++i) {
                     const int bb = tid * per + i;
@@ -580,14 +580,11 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
                 const int j = j0 + jj;
                 unsigned long long acc = 0ull;
                 const unsigned long long* w2 = reinterpret_cast<const unsigned long long*>(wq + j * 64);
+                float v[64];
+                tmem_ld64(lane_base + static_cast<uint32_t>(a * kN + j * 64), v);
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float v[32];
-                    tmem_ld32(lane_base + static_cast<uint32_t>(a * kN + j * 64 + hh * 32), v);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        acc = f2_fma(w2[hh * 16 + i], f2_pack(fmaxf(v[2 * i], 0.0f), fmaxf(v[2 * i + 1], 0.0f)), acc);
-                }
+                for (int i = 0; i < 32; ++i)
+                    acc = f2_fma(w2[i], f2_pack(fmaxf(v[2 * i], 0.0f), fmaxf(v[2 * i + 1], 0.0f)), acc);
                 const float2 pr = f2_unpack(acc);
                 res[jj] = kscale * (pr.x + pr.y);
             }

@@ -336,7 +336,10 @@ __device__ void select_topk_from_hist(Each each, const uint32_t* hist, int k, ui
     }
     __syncthreads();
     const uint32_t sortcap = static_cast<uint32_t>(min(cap, kTopkThreads * kMaxE));
-    if (count_ge <= sortcap) {
+    // sort everything at or above the boundary bin when that is no bigger a
+    // sort than the k winners need; otherwise refine the boundary bin first
+    const uint32_t direct = static_cast<uint32_t>(max(kTopkThreads, next_pow2(k)));
+    if (count_ge <= sortcap && count_ge <= direct) {
         // common case: everything at or above the boundary bin fits; one sort
         each([&](uint64_t c, bool v) {
             warp_append(buf, &ss->nsel, sortcap, c, v && static_cast<int>(comp_key(c) >> kHistShift) >= bstar);
