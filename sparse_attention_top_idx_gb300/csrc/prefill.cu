@@ -24,7 +24,7 @@ __host__ __device__ inline SelectPlan select_plan() {
 // One CTA per query row: histogram of the row's visible scores, then the exact
 // selection (the per-row top-k of ROCm/ATOM issue #1507, section "How it was
 // isolated", applied to the causal rows of _score_topk_prefill).
-__global__ void __launch_bounds__(kTopkThreads) prefill_select_kernel(const ScoreParams p) {
+__global__ void __launch_bounds__(kTopkThreads, 3) prefill_select_kernel(const ScoreParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     const SelectPlan sp = select_plan();
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + sp.hist_off);
@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kTopkThreads) prefill_select_kernel(const Scor
     auto each = [&](auto f) { walk_row(row, nvis, f); };
     each([&](uint64_t c, bool v) { hist_add_warp(hist, key_bin(comp_key(c)), v); });
     __syncthreads();
-    select_topk_from_hist<16>(each, hist, p.topk, sel, IDX_MAX_TOPK + kSelBcap, ss, oi, os);
+    select_topk_from_hist<8>(each, hist, p.topk, sel, IDX_MAX_TOPK + kSelBcap, ss, oi, os);
 }
 
 template <bool kFp8, int kBs>
