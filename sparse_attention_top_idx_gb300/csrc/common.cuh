@@ -210,6 +210,21 @@ __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void dsmem_st_u64(uint32_t addr, uint64_t v) {
     asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }
+__device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint2 dsmem_ld_v2(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint64_t dsmem_ld_u64(uint32_t addr) {
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    return static_cast<uint64_t>(v);
+}
 __device__ __forceinline__ void fence_acq_rel_cluster() {
     asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
@@ -226,6 +241,17 @@ __device__ __forceinline__ void dsmem_st_async_v4(uint32_t addr, uint4 v, uint32
 __device__ __forceinline__ void dsmem_st_async_u64(uint32_t addr, uint64_t v, uint32_t bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(addr), "l"(v),
                  "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void dsmem_st_async_u32(uint32_t addr, uint32_t v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+                 "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void dsmem_st_async_v2(uint32_t addr, uint32_t a, uint32_t b, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+                 "r"(a), "r"(b), "r"(bar)
                  : "memory");
 }
 

@@ -6,7 +6,7 @@ namespace dsaidx {
 
 namespace {
 
-constexpr int kDecodeCluster = 8;   // portable cluster size
+constexpr int kDecodeCluster = kCl;   // portable cluster size
 
 template <bool kFp8, int kBs>
 cudaError_t launch_decode_t(const idx_cache* c, const ScoreParams& p, cudaStream_t st) {

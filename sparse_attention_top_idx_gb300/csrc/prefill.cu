@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(kTopkThreads, 3) prefill_select_kernel(const S
     auto each = [&](auto f) { walk_row(row, nvis, f); };
     each([&](uint64_t c, bool v) { hist_add_warp(hist, key_bin(comp_key(c)), v); });
     __syncthreads();
-    select_topk_from_hist<8>(each, hist, p.topk, sel, IDX_MAX_TOPK + kSelBcap, ss, oi, os);
+    auto each_slow = [&](auto f) { walk_row_slow(row, nvis, f); };
+    select_topk_from_hist(each, each_slow, hist, p.topk, sel, IDX_MAX_TOPK + kSelBcap, ss, oi, os);
 }
 
 template <bool kFp8, int kBs>

@@ -29,29 +29,22 @@
 
 #include <cuda_bf16.h>
 
+#include "cluster_select.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "topk.cuh"
 
 namespace dsaidx {
 
-// Decode selection modes chosen by a cluster's leader.
-constexpr uint32_t kModeSmem = 1;     // candidates pushed into the leader's shared memory
-constexpr uint32_t kModeGlobal = 2;   // candidates published to the workspace
-
 struct KernelShared {
     uint32_t tmem_base;
     int abort;          // a role gave up on a bounded wait
     int bad;            // a block id failed its check
-    uint32_t ncand;     // leader: candidates received in shared memory
     uint32_t ticket;
     int unit_b, key_begin, key_end, seq_len, nrows, row0, nq;
     int seg, nseg;      // decode: segment of the sequence and segments in it
-    uint64_t cl_word;   // decode: boundary bin (low 32 bits) and selection mode
-                        // (high 32 bits) broadcast by the cluster leader
-    uint32_t cl_count;  // decode: candidates at or above the boundary (leader)
-    uint32_t cl_flag;   // decode: a CTA of the segment failed a device check
     int pos[kPrefillQT];
+    ClusterSmem cs;     // decode: the cluster selection's shared state
     SelectSmem sel;
     uint32_t grp[kThreads];   // prefill: group-count scan (first 256 threads)
 };
@@ -174,6 +167,44 @@ __device__ __forceinline__ void prep_queries(const uint8_t* raw, int nrows, uint
     }
 }
 
+// Sequence merge of a multi-segment decode sequence, run by the last CTA of
+// the sequence to finish: the top-k of the segments' sorted runs (`total`
+// composites, zero entries are padding) using the sequence histogram `gh` of
+// the runs' entries; then the per-sequence state is left zeroed for the next
+// call.  Out of line: it runs once per sequence, and keeping its code apart
+// keeps the kernel's common path compact.
+static __device__ __noinline__ void decode_merge(const uint64_t* runs, uint32_t total, uint32_t* gh, uint32_t* ctr,
+                                                 uint32_t* seqflag, uint32_t* seqcnt, uint32_t* hist, uint64_t* buf,
+                                                 int cap, SelectSmem* sel, int k, int32_t* oi, float* os) {
+    const int tid = threadIdx.x;
+    copy_hist_global(hist, gh);
+    const uint32_t flagged = __ldcg(seqflag);
+    __syncthreads();
+    if (flagged) {
+        for (int j = tid; j < k; j += kThreads) {
+            oi[j] = -1;
+            if (os) os[j] = -INFINITY;
+        }
+    } else {
+        // zero entries pad the runs
+        auto each = [&](auto f) { walk_global(runs, total, [&](uint64_t c, bool v) { f(c, v && c != 0ull); }); };
+        auto each_slow = [&](auto f) {
+            walk_global_slow(runs, total, [&](uint64_t c, bool v) { f(c, v && c != 0ull); });
+        };
+        select_topk_from_hist(each, each_slow, hist, k, buf, cap, sel, oi, os);
+    }
+    __syncthreads();
+    reinterpret_cast<uint4*>(gh)[tid] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(gh)[tid + 256] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(gh)[tid + 512] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(gh)[tid + 768] = make_uint4(0, 0, 0, 0);
+    if (tid == 0) {
+        *ctr = 0;
+        *seqflag = 0;
+        *seqcnt = 0;
+    }
+}
+
 // Two decode CTAs share an SM only at <= 124 registers per thread (measured
 // with the occupancy API on GB300: 126 already limits it to one), hence the
 // explicit cap for the decode instantiation.
@@ -197,8 +228,6 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
     constexpr int kBlocksPerTile = kTileKeys / kBs;
     constexpr int kKSteps = kFp8 ? 4 : 8;
     constexpr uint32_t kBlockTx = kFp8 ? (kBs * 128 + kBs * 4) : (kBs * 256);
-    constexpr int kDecodeSortE = 8;                         // leader sorts up to 2048 candidates
-    constexpr uint32_t kDecodeSortCap = kTopkThreads * kDecodeSortE;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -220,10 +249,8 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
     uint64_t* tempty = bars + 10;          // [2] epilogue -> MMA
     uint64_t* mdone = bars + 12;           // MMA drain at exit
     uint64_t* qbar = bars + 13;            // query rows staged
-    uint64_t* hbar = bars + 14;            // decode leader: every CTA's histogram added
-    uint64_t* bbar = bars + 15;            // decode: boundary bin broadcast received
-    uint64_t* gbar = bars + 16;            // decode leader: every CTA's candidates pushed
-    uint64_t* qready = bars + 17;          // decode: every rank's query rows written here
+    uint64_t* qready = bars + 14;          // decode: every rank's query rows written here
+    uint64_t* cbar = bars + 15;            // decode: [kClBars] cluster barriers of the selection
 
     const int tid = threadIdx.x;
     const int warp = warp_id(), lane = lane_id();
@@ -344,22 +371,19 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
         mbar_init(mdone, 1);
         mbar_init(qbar, 1);
         if constexpr (kDecode) {
-            mbar_init(hbar, p.cluster);
-            // bbar and qready complete when their bytes have arrived (st.async);
-            // gbar when the leader has announced the byte count and it arrived
-            mbar_init(bbar, 1);
-            mbar_init(gbar, 1);
+            // qready completes when the query bytes have arrived (st.async);
+            // each cluster barrier takes one arrive from every CTA
             mbar_init(qready, 1);
+            cluster_select_init(cbar);
         }
         fence_mbar_init();
         if constexpr (kDecode) {
-            mbar_arrive_expect_tx(bbar, 8);
             mbar_arrive_expect_tx(qready, 64 * (kFp8 ? 128 : 256) + 64 * 4);
+            cluster_select_expect(cbar);
         }
         ks->abort = 0;
         ks->bad = 0;
-        ks->ncand = 0;
-        ks->cl_flag = 0;
+        ks->cs.dead = 0;
     }
     if (warp == 1) {
         tmem_alloc(&ks->tmem_base, 2 * kN);
@@ -619,201 +643,75 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
         return;
     } else {
         // ------------------------------------------------ cluster top-k
-        // (1) the leader's histogram becomes the segment's histogram: every
-        //     other CTA adds its non-zero bins with DSMEM atomics.  (2) The
-        //     leader finds the boundary bin of the k-th best key and broadcasts
-        //     it.  (3) Every CTA pushes its keys at or above that bin into the
-        //     leader's shared memory, where one sort yields the top-k; or, for
-        //     sequences of several segments (or too many ties), publishes them
-        //     to the workspace and the last CTA of the sequence merges.
-        const int CL = p.cluster;
-        const uint32_t rank = cluster_rank();
+        // The segment's exact top-k by the whole cluster.  A one-segment
+        // sequence writes its outputs directly; a longer one writes each
+        // segment's sorted top-k (a run of k composites, zero-padded) and the
+        // run's histogram to the workspace, and the last CTA of the sequence
+        // to finish merges the runs.
         const int b = seq_b;
         const int n = key_end - key_begin;
         const int k = p.topk;
-        if (rank != 0) {
-            const uint32_t lh = dsmem_addr(hist, 0);
-            for (int i = tid * (kHistBins / kThreads); i < (tid + 1) * (kHistBins / kThreads); ++i) {
-                const uint32_t v = hist[i];
-                if (v) dsmem_red_add(lh + 4u * static_cast<uint32_t>(i), v);
-            }
-        }
-        if (tid == 0 && (ks->bad || ks->abort)) dsmem_red_add(dsmem_addr(&ks->cl_flag, 0), 1u);
-        // one release per CTA: the barrier orders every thread's remote adds
-        // before thread 0's cluster-scope fence and arrive
-        __syncthreads();
-        if (tid == 0) {
-            fence_acq_rel_cluster();
-            mbar_arrive_remote(dsmem_addr(hbar, 0));
-        }
-        if (rank == 0) {
-            if (!mbar_wait_cluster(hbar, 0, status)) ks->abort = 1;
-            block_find_suffix(hist, kHistBins, static_cast<uint32_t>(k), ks->sel.scratch, &ks->sel.bnd);
-            const uint32_t count_ge = ks->sel.bnd.above + ks->sel.bnd.at;
-            const uint32_t mode = (ks->nseg == 1 && count_ge <= kDecodeSortCap) ? kModeSmem : kModeGlobal;
-            if (tid == 0) {
-                ks->cl_count = count_ge;
-                // the pushed candidates complete gbar: announce their bytes
-                // before any CTA can learn the boundary
-                if (mode == kModeSmem) mbar_arrive_expect_tx(gbar, count_ge * 8u);
-            }
-            __syncthreads();
-            if (tid < CL) {
-                const uint64_t word = (static_cast<uint64_t>(mode) << 32) | static_cast<uint32_t>(ks->sel.bnd.bin);
-                dsmem_st_async_u64(dsmem_addr(&ks->cl_word, static_cast<uint32_t>(tid)), word,
-                                   dsmem_addr(bbar, static_cast<uint32_t>(tid)));
-            }
-        }
-        if (!mbar_wait_cluster(bbar, 0, status)) ks->abort = 1;
-        const int bstar = static_cast<int>(static_cast<uint32_t>(ks->cl_word));   // -1: fewer than k keys
-        const uint32_t mode = static_cast<uint32_t>(ks->cl_word >> 32);
         const int nround = (n + kThreads - 1) / kThreads * kThreads;
-
-        if (mode == kModeSmem) {
-            // count this CTA's keys at or above the boundary, reserve that many
-            // slots of the leader's buffer with one remote atomic, and push them
-            // as st.async counted on the leader's gbar
-            uint32_t mine = 0;
-            for (int i = tid; i < n; i += kThreads)
-                mine += static_cast<int>(key_bin(score_key(cscores[i]))) >= bstar ? 1u : 0u;
-            for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-            if (lane == 0) ks->sel.scratch[warp] = mine;
-            __syncthreads();
-            if (tid == 0) {
-                uint32_t tot = 0;
-                for (int w8 = 0; w8 < kThreads / 32; ++w8) tot += ks->sel.scratch[w8];
-                ks->sel.nsel = 0;
-                ks->ticket = tot ? dsmem_atom_add(dsmem_addr(&ks->ncand, 0), tot) : 0u;
-            }
-            __syncthreads();
-            const uint32_t lbuf = dsmem_addr(a_tiles, 0) + 8u * ks->ticket;
-            const uint32_t lgbar = dsmem_addr(gbar, 0);
+        const bool single = ks->nseg == 1;
+        int32_t* oi = p.out_idx + static_cast<int64_t>(b) * k;
+        float* os = p.out_score ? p.out_score + static_cast<int64_t>(b) * k : nullptr;
+        uint64_t* run = p.cand + static_cast<int64_t>(b) * p.cand_cap + static_cast<int64_t>(ks->seg) * k;
+        uint32_t* gh = p.ghist + static_cast<int64_t>(b) * kHistBins;
+        uint64_t* lists = reinterpret_cast<uint64_t*>(a_tiles);   // 3 x kClCap composites
+        const ClusterBufs B{hist,
+                            reinterpret_cast<uint32_t*>(qtile),
+                            reinterpret_cast<uint32_t*>(lists),
+                            reinterpret_cast<uint32_t*>(lists + kClCap),
+                            lists,
+                            lists + kClCap,
+                            lists + 2 * kClCap,
+                            cbar};
+        auto walk = [&](auto f) {
             for (int i = tid; i < nround; i += kThreads) {
-                uint32_t kk = 0;
-                bool take = false;
-                if (i < n) {
-                    kk = score_key(cscores[i]);
-                    take = static_cast<int>(key_bin(kk)) >= bstar;
-                }
-                const unsigned m = __ballot_sync(0xffffffffu, take);
-                if (m) {
-                    const int leader = __ffs(m) - 1;
-                    uint32_t base = 0;
-                    if (lane == leader) base = atomicAdd(&ks->sel.nsel, static_cast<uint32_t>(__popc(m)));
-                    base = __shfl_sync(0xffffffffu, base, leader);
-                    if (take) {
-                        const uint32_t pos = base + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
-                        if (ks->ticket + pos < kDecodeSortCap)
-                            dsmem_st_async_u64(lbuf + 8u * pos, make_comp(kk, key_begin + i), lgbar);
-                    }
-                }
+                const bool v = i < n;
+                f(make_comp(v ? score_key(cscores[i]) : 0u, key_begin + i), v);
             }
-            if (rank != 0) return;   // nothing touches this CTA's shared memory any more
-            if (!mbar_wait_cluster(gbar, 0, status)) ks->abort = 1;
-            __syncthreads();
-            int32_t* oi = p.out_idx + static_cast<int64_t>(b) * k;
-            float* os = p.out_score ? p.out_score + static_cast<int64_t>(b) * k : nullptr;
-            const int cnt = static_cast<int>(min(ks->cl_count, kDecodeSortCap));
-            if (ks->cl_flag || ks->abort) {
-                for (int j = tid; j < k; j += kThreads) {
-                    oi[j] = -1;
-                    if (os) os[j] = -INFINITY;
-                }
-                return;
+        };
+        auto emit = [&](int r, uint64_t c) {
+            if (single) {
+                oi[r] = comp_index(c);
+                if (os) os[r] = key_score(comp_key(c));
+            } else {
+                run[r] = c;
+                atomicAdd(&gh[key_bin(comp_key(c))], 1u);
             }
-            uint64_t* buf = reinterpret_cast<uint64_t*>(a_tiles);
-            block_sort_desc_n<kDecodeSortE>(buf, cnt);
-            const int nsel = min(k, cnt);
-            for (int j = tid; j < k; j += kThreads) {
-                if (j < nsel) {
-                    const uint64_t c = buf[j];
-                    oi[j] = comp_index(c);
-                    if (os) os[j] = key_score(comp_key(c));
-                } else {
+        };
+        const int count = cluster_select(walk, emit, B, k, ks->bad != 0 || ks->abort != 0, &ks->cs, status);
+        const bool first = cluster_rank() == 0;
+        if (single) {
+            if (first) {
+                for (int j = max(count, 0) + tid; j < k; j += kThreads) {
                     oi[j] = -1;
                     if (os) os[j] = -INFINITY;
                 }
             }
             return;
         }
-
-        // ------------------------------------------------ workspace path
-        // Publish every key in bins >= T (T: the segment's boundary bin, a lower
-        // bound on the sequence's k-th best) and its histogram counts, then the
-        // last CTA of the sequence selects from the published set.
-        const int T = max(bstar, 0);
-        uint32_t* gh = p.ghist + static_cast<int64_t>(b) * kHistBins;
-        const int nch = ks->nseg * CL;     // CTAs of the sequence
-        // count this CTA's keys in bins >= T (the leader's histogram holds the
-        // whole segment, so count from the scores), reserve that many slots of
-        // the sequence's candidate buffer with one atomic, then write them
-        {
-            uint32_t mine = 0;
-            for (int i = tid; i < n; i += kThreads)
-                mine += static_cast<int>(key_bin(score_key(cscores[i]))) >= T ? 1u : 0u;
-            for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-            if (lane == 0) ks->sel.scratch[warp] = mine;
-            __syncthreads();
-            if (tid == 0) {
-                uint32_t tot = 0;
-                for (int w8 = 0; w8 < kThreads / 32; ++w8) tot += ks->sel.scratch[w8];
-                ks->sel.nsel = 0;
-                ks->ticket = tot ? atomicAdd(p.seqcnt + b, tot) : 0u;   // base slot of this CTA
+        if (first) {
+            if (count < 0) {
+                if (tid == 0) atomicOr(p.seqflag + b, 1u);
+            } else {
+                for (int j = count + tid; j < k; j += kThreads) run[j] = 0ull;
             }
-            __syncthreads();
         }
-        uint64_t* cl = p.cand + static_cast<int64_t>(b) * p.cand_cap + ks->ticket;
-        for (int i = tid; i < nround; i += kThreads) {
-            uint32_t kk = 0;
-            bool take = false;
-            if (i < n) {
-                kk = score_key(cscores[i]);
-                take = static_cast<int>(key_bin(kk)) >= T;
-            }
-            warp_append(cl, &ks->sel.nsel, 0xFFFFFFFFu, make_comp(kk, key_begin + i), take);
-            hist_add_warp(gh, key_bin(kk), take);   // the published set's histogram
-        }
+        // the last CTA of the sequence to finish merges
         __threadfence();
         __syncthreads();
-        if (tid == 0) {
-            if (ks->bad || ks->abort) atomicOr(p.seqflag + b, 1u);
-            __threadfence();
-            ks->ticket = atomicAdd(p.ctr + b, 1u);
-        }
+        if (tid == 0) ks->ticket = atomicAdd(p.ctr + b, 1u);
         __syncthreads();
-        if (ks->ticket != static_cast<uint32_t>(nch - 1)) return;
+        if (ks->ticket != static_cast<uint32_t>(ks->nseg * kCl - 1)) return;
 
         // ------------------------------------------------ sequence merge (last CTA)
         __threadfence();
-        copy_hist_global(hist, gh);
-        const uint32_t flagged = __ldcg(p.seqflag + b);
-        const uint32_t total = __ldcg(p.seqcnt + b);
-        __syncthreads();
-        int32_t* oi = p.out_idx + static_cast<int64_t>(b) * k;
-        float* os = p.out_score ? p.out_score + static_cast<int64_t>(b) * k : nullptr;
-        if (flagged) {
-            for (int j = tid; j < k; j += kThreads) {
-                oi[j] = -1;
-                if (os) os[j] = -INFINITY;
-            }
-        } else {
-            uint64_t* buf = reinterpret_cast<uint64_t*>(a_tiles);
-            const int cap = kStages * plan.a_stage_bytes / 8;
-            const uint64_t* L = p.cand + static_cast<int64_t>(b) * p.cand_cap;
-            auto each = [&](auto f) { walk_global(L, total, f); };
-            select_topk_from_hist<kDecodeSortE>(each, hist, k, buf, cap, &ks->sel, oi, os);
-        }
-        // leave the per-sequence state zeroed for the next call
-        __syncthreads();
-        reinterpret_cast<uint4*>(gh)[tid] = make_uint4(0, 0, 0, 0);
-        reinterpret_cast<uint4*>(gh)[tid + 256] = make_uint4(0, 0, 0, 0);
-        reinterpret_cast<uint4*>(gh)[tid + 512] = make_uint4(0, 0, 0, 0);
-        reinterpret_cast<uint4*>(gh)[tid + 768] = make_uint4(0, 0, 0, 0);
-        if (tid == 0) {
-            p.ctr[b] = 0;
-            p.seqflag[b] = 0;
-            p.seqcnt[b] = 0;
-        }
+        decode_merge(p.cand + static_cast<int64_t>(b) * p.cand_cap,
+                     static_cast<uint32_t>(ks->nseg) * static_cast<uint32_t>(k), gh, p.ctr + b, p.seqflag + b,
+                     p.seqcnt + b, hist, reinterpret_cast<uint64_t*>(a_tiles), kStages * plan.a_stage_bytes / 8,
+                     &ks->sel, k, oi, os);
     }
 }
 

@@ -4,8 +4,7 @@
 // of composites is "higher score first, then lower index", the tie rule of the
 // library, and composites are unique within one query row.  Selection works on
 // a 4096-bin histogram of the top 12 bits of score_key followed by exact radix
-// refinement of the boundary bin, and finishes with a bitonic sort of the k
-// winners.
+// refinement of the boundary bin, and finishes with a sort of the k winners.
 #pragma once
 
 #include "common.cuh"
@@ -23,15 +22,12 @@ __device__ __forceinline__ int32_t comp_index(uint64_t c) {
 __device__ __forceinline__ uint32_t comp_key(uint64_t c) { return static_cast<uint32_t>(c >> 32); }
 __device__ __forceinline__ uint32_t key_bin(uint32_t key) { return key >> kHistShift; }
 
-// Warp-aggregated shared-memory histogram increment (one atomic per distinct
-// bin in the warp).  Every lane of the warp must call it; `valid` masks lanes.
+// Shared-memory histogram increment for the lanes with `valid`.  A plain
+// atomic per lane: on sm_103a this measured about three times faster than
+// first aggregating equal bins with a warp match, even when most lanes of a
+// warp share a few bins.
 __device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, bool valid) {
-    unsigned active = __ballot_sync(0xffffffffu, valid);
-    if (valid) {
-        unsigned peers = __match_any_sync(active, bin);
-        if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(peers) - 1))
-            atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
-    }
+    if (valid) atomicAdd(&hist[bin], 1u);
 }
 
 struct Boundary {
@@ -179,6 +175,25 @@ __device__ __forceinline__ void walk_row(const float* row, int n, F f) {
     }
 }
 
+// Compact walks over the same candidates, one load per iteration: for the
+// rare paths that walk the candidates again (small code, slow).
+template <class F>
+__device__ __forceinline__ void walk_global_slow(const uint64_t* a, uint32_t n, F f) {
+#pragma unroll 1
+    for (uint32_t b0 = 0; b0 < n; b0 += kTopkThreads) {
+        const uint32_t i = b0 + threadIdx.x;
+        f(i < n ? static_cast<uint64_t>(__ldcg(reinterpret_cast<const unsigned long long*>(a) + i)) : 0ull, i < n);
+    }
+}
+template <class F>
+__device__ __forceinline__ void walk_row_slow(const float* row, int n, F f) {
+#pragma unroll 1
+    for (int b0 = 0; b0 < n; b0 += kTopkThreads) {
+        const int i = b0 + static_cast<int>(threadIdx.x);
+        f(make_comp(score_key(i < n ? __ldcg(row + i) : 0.0f), i), i < n);
+    }
+}
+
 // Exact refinement inside one bin: among the candidate set X (all composites
 // whose top 12 bits equal `bin`), find the composite threshold thr such that
 // exactly m members of X are >= thr.  `each` walks a superset of X (members
@@ -188,9 +203,9 @@ __device__ uint64_t radix_refine(Each each, int bin, uint32_t m, SelectSmem* ss)
     uint64_t prefix = static_cast<uint64_t>(bin) << 52;
     uint64_t mask = 0xFFFull << 52;
     uint32_t need = m;
-    const int shifts[7] = {44, 36, 28, 20, 12, 4, 0};
+#pragma unroll 1
     for (int pass = 0; pass < 7; ++pass) {
-        const int sh = shifts[pass];
+        const int sh = pass < 6 ? 44 - 8 * pass : 0;   // 8-bit digits, then the last 4 bits
         const uint64_t dmask = (pass == 6) ? 0xFull : 0xFFull;
         ss->hist256[threadIdx.x] = 0;
         __syncthreads();
@@ -235,19 +250,22 @@ __device__ __forceinline__ void bitonic_sort_desc(uint64_t* a, int n) {
 // owns positions t*E .. t*E+E-1).  Bitonic network: compare-exchanges between
 // a thread's own registers, then across lanes with warp shuffles, and through
 // shared memory (two block barriers a stage) only for strides that cross
-// warps: for 4096 keys, 6 of the 78 stages.
+// warps: for 4096 keys, 6 of the 78 stages.  In shared memory position
+// t*E + e lives at word e*256 + t, so that the 32 lanes of a warp touch 32
+// consecutive words (no bank conflicts) in every exchange.
 // ---------------------------------------------------------------------------
 template <int E, int SIZE, int STRIDE>
 __device__ __forceinline__ void bsort_stage(uint64_t (&v)[E], uint64_t* a) {
     const int t = threadIdx.x;
     if constexpr (STRIDE >= 32 * E) {
+        // partner of position t*E + e is (t ^ STRIDE/E)*E + e: same e, other thread
 #pragma unroll
-        for (int e = 0; e < E; ++e) a[t * E + e] = v[e];
+        for (int e = 0; e < E; ++e) a[e * kTopkThreads + t] = v[e];
         __syncthreads();
 #pragma unroll
         for (int e = 0; e < E; ++e) {
             const int i = t * E + e;
-            const uint64_t p = a[i ^ STRIDE];
+            const uint64_t p = a[e * kTopkThreads + (t ^ (STRIDE / E))];
             const bool keep_max = ((i & STRIDE) == 0) == ((i & SIZE) == 0);
             v[e] = keep_max ? (v[e] > p ? v[e] : p) : (v[e] < p ? v[e] : p);
         }
@@ -285,11 +303,13 @@ __device__ __forceinline__ void bsort_sizes(uint64_t (&v)[E], uint64_t* a) {
     if constexpr (SIZE < kTopkThreads * E) bsort_sizes<E, SIZE * 2>(v, a);
 }
 // Sorts a[0 .. 256*E) in place (shared memory), descending.  All 256 threads.
+// The input order is immaterial, so each thread loads the conflict-free words
+// e*256 + t; only the final store writes position order.
 template <int E>
 __device__ __forceinline__ void block_sort_desc(uint64_t* a) {
     uint64_t v[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) v[e] = a[threadIdx.x * E + e];
+    for (int e = 0; e < E; ++e) v[e] = a[e * kTopkThreads + threadIdx.x];
     bsort_sizes<E, 2>(v, a);
     __syncthreads();
 #pragma unroll
@@ -311,6 +331,131 @@ __device__ __forceinline__ void block_sort_desc_n(uint64_t* a, int n) {
     else block_sort_desc<kMaxE>(a);
 }
 
+// ---------------------------------------------------------------------------
+// Rank sort, descending, of up to 256 * E composites (all 256 threads).
+// Each warp sorts a run of 32 * E composites in registers (bitonic network,
+// E per lane, lane l holding run positions l*E .. l*E+E-1: compare-exchanges
+// between a lane's registers, then across lanes by shuffles, no block
+// barriers).  The runs go to shared memory and every composite's final
+// position is its position in its own run plus, for each of the seven other
+// runs, the number of its members that are larger (binary searches).
+// Composites are unique, so the positions are a permutation; zero is the
+// padding value and is never written back.  This code runs once per block
+// from a cold instruction cache, so its loops stay rolled: the code is small
+// and each instruction is fetched once, then re-issued from the cache.
+// ---------------------------------------------------------------------------
+
+// Address of run position j in a run stored lane-transposed (position
+// l*E + e of a warp's registers at word e*32 + l).
+template <int E>
+__device__ __forceinline__ int run_slot(int j) {
+    return (j % E) * 32 + j / E;
+}
+
+template <int E>
+__device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[E], int lane) {
+#pragma unroll 1
+    for (int size = 2; size <= 32 * E; size <<= 1) {
+        // strides >= E: the partner is register e of lane ^ stride/E; the
+        // direction depends on the lane only
+#pragma unroll 1
+        for (int stride = size >> 1; stride >= E; stride >>= 1) {
+            const bool lower = (lane & (stride / E)) == 0;
+            const bool desc = (lane & (size / E)) == 0;
+            const bool keep_max = (lower == desc);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const uint64_t p =
+                    __shfl_xor_sync(0xffffffffu, static_cast<unsigned long long>(v[e]), stride / E);
+                v[e] = ((v[e] > p) == keep_max) ? v[e] : p;
+            }
+        }
+        // strides < E: both partners in this lane's registers
+#pragma unroll
+        for (int stride = E / 2; stride >= 1; stride >>= 1) {
+            if (2 * stride <= size) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    if ((e & stride) == 0) {
+                        const bool desc = ((lane * E + e) & size) == 0;
+                        const uint64_t x = v[e], y = v[e + stride];
+                        if ((x < y) == desc) {
+                            v[e] = y;
+                            v[e + stride] = x;
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Sorts a[0 .. n) descending, n <= 256 * E; `runs` is scratch for 256 * E
+// composites that must not overlap a.
+template <int E>
+__device__ __forceinline__ void block_rank_sort(uint64_t* a, int n, uint64_t* runs) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    constexpr int R = 32 * E;
+    {
+        uint64_t v[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int i = w * R + e * 32 + lane;   // any assignment will do: read conflict-free
+            v[e] = i < n ? a[i] : 0ull;
+        }
+        warp_sort_desc<E>(v, lane);
+        uint64_t* mine = runs + w * R;
+#pragma unroll
+        for (int e = 0; e < E; ++e) mine[e * 32 + lane] = v[e];
+    }
+    __syncthreads();
+    // final position = own run position + larger members of the 7 other runs
+    // (seven branch-free binary searches advanced together)
+#pragma unroll 1
+    for (int e = 0; e < E; ++e) {
+        const int j0 = lane * E + e;
+        const uint64_t x = runs[w * R + run_slot<E>(j0)];
+        if (x == 0ull) continue;     // padding (zeros sort last in each run)
+        int pos[7];
+#pragma unroll
+        for (int o = 0; o < 7; ++o) pos[o] = 0;
+#pragma unroll 1
+        for (int step = R / 2; step >= 1; step >>= 1) {
+#pragma unroll
+            for (int o = 0; o < 7; ++o) {
+                const uint64_t* other = runs + ((w + 1 + o) & 7) * R;
+                if (other[run_slot<E>(pos[o] + step - 1)] > x) pos[o] += step;
+            }
+        }
+        int rank = j0;
+#pragma unroll
+        for (int o = 0; o < 7; ++o) {
+            const uint64_t* other = runs + ((w + 1 + o) & 7) * R;
+            rank += pos[o] + ((other[run_slot<E>(pos[o])] > x) ? 1 : 0);
+        }
+        a[rank] = x;
+    }
+    __syncthreads();
+}
+
+// Sorts a[0 .. n) descending for n <= 256 * kMaxE (zero entries are padding
+// and must not occur among the n); `runs`: scratch for 256 * kMaxE
+// composites, disjoint from a.
+template <int kMaxE>
+__device__ __forceinline__ void block_sort_desc_r(uint64_t* a, int n, uint64_t* runs) {
+    if (n <= 256) block_rank_sort<1>(a, n, runs);
+    else if (n <= 512 || kMaxE < 4) block_rank_sort<(kMaxE < 2 ? kMaxE : 2)>(a, n, runs);
+    else if (n <= 1024 || kMaxE < 8) block_rank_sort<(kMaxE < 4 ? kMaxE : 4)>(a, n, runs);
+    else block_rank_sort<kMaxE>(a, n, runs);
+}
+
+// One out-of-line copy per kernel: the kernels sort from several places, each
+// once per block and from a cold instruction cache, so sharing one copy keeps
+// their code (and the instruction fetches) small.
+static __device__ __noinline__ void block_sort_any(uint64_t* a, int n, uint64_t* runs) {
+    block_sort_desc_r<8>(a, n, runs);
+}
+
 __device__ __forceinline__ int next_pow2(int x) {
     int p = 1;
     while (p < x) p <<= 1;
@@ -318,83 +463,69 @@ __device__ __forceinline__ int next_pow2(int x) {
 }
 
 // Final selection of one query row from a candidate set whose 4096-bin
-// histogram `hist` (shared) is exact.  `each` walks every candidate.  buf:
-// shared buffer of cap >= 2048 + (boundary room) composites; up to 256 * kMaxE
-// candidates at or above the boundary bin are selected by one sort.  Writes the k outputs (descending,
-// -1 / -inf padded).  Called by all 256 threads.
-template <int kMaxE, class Each>
-__device__ void select_topk_from_hist(Each each, const uint32_t* hist, int k, uint64_t* buf, int cap,
-                                      SelectSmem* ss, int32_t* out_idx, float* out_score) {
+// histogram `hist` (shared) is exact.  each(f) walks every candidate once
+// (the fast, unrolled walk: called at one place); each_slow(f) walks them
+// again with compact code, only when the boundary bin overflows shared
+// memory.  buf: shared buffer of cap >= 4096 composites: [0, 2048) collects
+// the selection, the rest first the boundary bin, then the sort's scratch.
+// Writes the k outputs (descending, -1 / -inf padded).  All 256 threads.
+template <class Each, class EachSlow>
+__device__ void select_topk_from_hist(Each each, EachSlow each_slow, const uint32_t* hist, int k, uint64_t* buf,
+                                      int cap, SelectSmem* ss, int32_t* out_idx, float* out_score) {
     const int tid = threadIdx.x;
     block_find_suffix(hist, kHistBins, static_cast<uint32_t>(k), ss->scratch, &ss->bnd);
     const int bstar = ss->bnd.bin;
-    const uint32_t above = ss->bnd.above;
-    const uint32_t count_ge = above + ss->bnd.at;     // candidates in bins >= bstar
+    const uint32_t above = ss->bnd.above;              // the total when bstar = -1
+    const uint32_t count_ge = above + ss->bnd.at;      // candidates in bins >= bstar
     if (tid == 0) {
         ss->nsel = 0;
         ss->nbnd = 0;
     }
     __syncthreads();
-    const uint32_t sortcap = static_cast<uint32_t>(min(cap, kTopkThreads * kMaxE));
-    // sort everything at or above the boundary bin when that is no bigger a
-    // sort than the k winners need; otherwise refine the boundary bin first
-    const uint32_t direct = static_cast<uint32_t>(max(kTopkThreads, next_pow2(k)));
-    if (count_ge <= sortcap && count_ge <= direct) {
-        // common case: everything at or above the boundary bin fits; one sort
-        each([&](uint64_t c, bool v) {
-            warp_append(buf, &ss->nsel, sortcap, c, v && static_cast<int>(comp_key(c) >> kHistShift) >= bstar);
-        });
-        __syncthreads();
-        block_sort_desc_n<kMaxE>(buf, static_cast<int>(count_ge));
-        const int nsel = min(k, static_cast<int>(count_ge));
-        for (int j = tid; j < k; j += kTopkThreads) {
-            if (j < nsel) {
-                const uint64_t c = buf[j];
-                out_idx[j] = comp_index(c);
-                if (out_score) out_score[j] = key_score(comp_key(c));
-            } else {
-                out_idx[j] = -1;
-                if (out_score) out_score[j] = -INFINITY;
-            }
-        }
-        return;
-    }
-    // many candidates share the boundary bin: refine it by radix passes
-    uint64_t* sel = buf;
+    // one pass: bins above the boundary to buf, the boundary bin to bndbuf
     uint64_t* bndbuf = buf + IDX_MAX_TOPK;
-    const int bcap = cap - IDX_MAX_TOPK;
-    // gather: bins above the boundary go straight to sel, the boundary bin to bndbuf
+    const uint32_t bcap = static_cast<uint32_t>(cap - IDX_MAX_TOPK);
     each([&](uint64_t c, bool v) {
         const int b = static_cast<int>(comp_key(c) >> kHistShift);
-        warp_append(sel, &ss->nsel, static_cast<uint32_t>(k), c, v && b > bstar);
-        warp_append(bndbuf, &ss->nbnd, static_cast<uint32_t>(bcap), c, v && b == bstar);
+        warp_append(buf, &ss->nsel, static_cast<uint32_t>(k), c, v && b > bstar);
+        warp_append(bndbuf, &ss->nbnd, bcap, c, v && b == bstar);
     });
     __syncthreads();
+    int nsort = static_cast<int>(above);   // composites to sort (the first k are output)
     if (bstar >= 0) {
-        const uint32_t m = static_cast<uint32_t>(k) - above;
-        const uint32_t nb = ss->nbnd;
-        const bool fits = nb <= static_cast<uint32_t>(bcap);
-        if (fits && nb == m) {
-            for (uint32_t i = tid; i < nb; i += kTopkThreads) sel[above + i] = bndbuf[i];
+        const uint32_t m = static_cast<uint32_t>(k) - above;   // needed from the boundary bin
+        const uint32_t nb = ss->bnd.at;
+        const uint32_t direct = static_cast<uint32_t>(max(kTopkThreads, next_pow2(k)));
+        if (nb <= bcap && (nb == m || count_ge <= direct)) {
+            // the whole boundary bin joins the sort
+            for (uint32_t i = tid; i < nb; i += kTopkThreads) buf[above + i] = bndbuf[i];
+            nsort = static_cast<int>(count_ge);
         } else {
-            auto each_bnd = [&](auto f) { walk_smem(bndbuf, nb, f); };
-            const uint64_t thr = fits ? radix_refine(each_bnd, bstar, m, ss) : radix_refine(each, bstar, m, ss);
+            // refine the boundary bin to its m best by radix passes
+            uint64_t thr;
+            if (nb <= bcap) {
+                auto each_bnd = [&](auto f) { walk_smem(bndbuf, nb, f); };
+                thr = radix_refine(each_bnd, bstar, m, ss);
+            } else {
+                thr = radix_refine(each_slow, bstar, m, ss);
+            }
             if (tid == 0) ss->nsel = above;
             __syncthreads();
             auto take = [&](uint64_t c, bool v) {
                 const bool in = v && static_cast<int>(comp_key(c) >> kHistShift) == bstar && c >= thr;
-                warp_append(sel, &ss->nsel, static_cast<uint32_t>(k), c, in);
+                warp_append(buf, &ss->nsel, static_cast<uint32_t>(k), c, in);
             };
-            if (fits) each_bnd(take);
-            else each(take);
+            if (nb <= bcap) walk_smem(bndbuf, nb, take);
+            else each_slow(take);
+            nsort = k;
         }
         __syncthreads();
     }
-    const int nsel = (bstar >= 0) ? k : static_cast<int>(above);
-    block_sort_desc_n<8>(sel, nsel);
+    block_sort_any(buf, nsort, bndbuf);
+    const int nout = min(k, nsort);
     for (int j = tid; j < k; j += kTopkThreads) {
-        if (j < nsel) {
-            uint64_t c = sel[j];
+        if (j < nout) {
+            const uint64_t c = buf[j];
             out_idx[j] = comp_index(c);
             if (out_score) out_score[j] = key_score(comp_key(c));
         } else {
