@@ -148,6 +148,10 @@ __device__ __forceinline__ void block_suffix_find_reg(const uint32_t (&v)[PER], 
 
 // The cluster's exact top-k.  walk(f) calls f(composite, valid) over this
 // CTA's composites (valid ones are never 0) with warp-uniform trip counts;
+// collect0(kthr, dst, cap, seg, wsum) collects the composites whose score key
+// is >= kthr into dst the way block_collect_warp does (seg: scratch) and
+// returns their number -- a faster first pass than walk where the caller can
+// test the 32-bit key alone;
 // B.hist must hold their top-12-bit histogram.  emit(r, c) receives every
 // candidate c of this CTA whose rank r among the cluster's composites is
 // below k (each rank in [0, min(k, count)) exactly once over the cluster).
@@ -155,9 +159,9 @@ __device__ __forceinline__ void block_suffix_find_reg(const uint32_t (&v)[PER], 
 // holds fewer than k composites), or -1 when a CTA of the cluster reported
 // `flagged` (every CTA returns -1 then) or a wait timed out.  Called by all
 // 256 threads of every CTA of the cluster.
-template <class Walk, class Emit>
-__device__ int cluster_select(Walk walk, Emit emit, const ClusterBufs& B, int k, bool flagged, ClusterSmem* cs,
-                              int32_t* status) {
+template <class Walk, class Collect0, class Emit>
+__device__ int cluster_select(Walk walk, Collect0 collect0, Emit emit, const ClusterBufs& B, int k, bool flagged,
+                              ClusterSmem* cs, int32_t* status) {
     const int tid = threadIdx.x;
     const uint32_t rank = cluster_rank();
 
@@ -218,6 +222,18 @@ __device__ int cluster_select(Walk walk, Emit emit, const ClusterBufs& B, int k,
     uint64_t mask = 0xFFFull << 52;
     uint32_t need = static_cast<uint32_t>(k) - min(above, static_cast<uint32_t>(k));
     uint32_t count = above + at;
+    // this CTA's composites >= thr, collected once: when they fit, the
+    // refinement levels and the final filter read this list instead of
+    // walking every composite again
+    // (thr has zero low 52 bits here: the key alone decides)
+    const uint32_t n0 = collect0(bstar >= 0 ? static_cast<uint32_t>(bstar) << 20 : 0u, B.list,
+                                 static_cast<uint32_t>(kClCap), B.runs, cs->wsum);
+    const bool pre = n0 <= static_cast<uint32_t>(kClCap);
+    auto cands = [&](auto f) {
+        if (pre) walk_smem(B.list, n0, f);
+        else walk(f);
+    };
+    const uint64_t thr0 = thr;
 #pragma unroll 1
     for (int lvl = 0; count > static_cast<uint32_t>(kClCap) && lvl < kClLevels; ++lvl) {
         // refine: histogram of the next digit over the boundary group
@@ -225,7 +241,7 @@ __device__ int cluster_select(Walk walk, Emit emit, const ClusterBufs& B, int k,
         const uint64_t dmask = lvl < 6 ? 0xFFull : 0xFull;
         B.mine[tid] = 0;
         __syncthreads();
-        walk([&](uint64_t c, bool v) {
+        cands([&](uint64_t c, bool v) {
             hist_add_warp(B.mine, static_cast<uint32_t>((c >> sh) & dmask), v && (c & mask) == thr);
         });
         __syncthreads();
@@ -249,15 +265,22 @@ __device__ int cluster_select(Walk walk, Emit emit, const ClusterBufs& B, int k,
 
     // (2) this CTA's candidates: their number to every CTA, then sorted, then
     //     the list to every CTA
-    if (tid == 0) cs->nloc = 0;
-    __syncthreads();
-    walk([&](uint64_t c, bool v) { warp_append(B.list, &cs->nloc, kClCap, c, v && c >= thr); });
-    __syncthreads();
-    const int nr = min(static_cast<int>(cs->nloc), kClCap);
+    uint64_t* mylist = B.list;   // sorted in place, then pushed and ranked
+    uint64_t* scratch = B.runs;
+    uint32_t nfound = n0;
+    if (!(pre && thr == thr0)) {
+        // refined (or the first collection overflowed): collect again
+        mylist = pre ? B.runs : B.list;
+        scratch = pre ? B.list : B.runs;
+        // segment scratch: gath receives nothing before this CTA pushes its count
+        nfound = block_collect_warp(cands, [&](uint64_t c) { return c >= thr; }, mylist, kClCap,
+                                    pre ? B.gath : B.runs, cs->wsum);
+    }
+    const int nr = min(static_cast<int>(nfound), kClCap);
     if (tid < kCl)
         dsmem_st_async_u32(dsmem_addr(&cs->lcnt[rank], static_cast<uint32_t>(tid)), static_cast<uint32_t>(nr),
                            dsmem_addr(&B.cbar[kClBarCount], static_cast<uint32_t>(tid)));
-    block_sort_any(B.list, nr, B.runs);
+    block_sort_any(mylist, nr, scratch);
     if (!cl_wait(&B.cbar[kClBarCount], status, cs)) return -1;
     int off[kCl + 1];
     off[0] = 0;
@@ -278,7 +301,7 @@ __device__ int cluster_select(Walk walk, Emit emit, const ClusterBufs& B, int k,
         for (int j = tid; j < mine_n * kCl; j += kTopkThreads) {
             const int e = j / kCl;
             const uint32_t q = static_cast<uint32_t>(j % kCl);
-            dsmem_st_async_u64(dsmem_addr(B.gath + mine_off + e, q), B.list[e], dsmem_addr(&B.cbar[kClBarList], q));
+            dsmem_st_async_u64(dsmem_addr(B.gath + mine_off + e, q), mylist[e], dsmem_addr(&B.cbar[kClBarList], q));
         }
     }
     if (!cl_wait(&B.cbar[kClBarList], status, cs)) return -1;
@@ -290,7 +313,7 @@ __device__ int cluster_select(Walk walk, Emit emit, const ClusterBufs& B, int k,
     const int iters = 32 - __clz(maxlen);   // binary-search steps for the longest list
 #pragma unroll 1
     for (int i = tid; i < nr; i += kTopkThreads) {
-        const uint64_t x = B.list[i];
+        const uint64_t x = mylist[i];
         int lo[kCl], len[kCl];
 #pragma unroll
         for (int q = 0; q < kCl; ++q) {

@@ -91,7 +91,7 @@ __host__ __device__ inline SmemPlan make_plan(bool fp8, int qt, int chunk) {
     p.raw_off = o;     o += raw_bytes;
     p.bid_off = o;     o += kBidWindow * 4;  // prefetched block ids
     p.misc_off = o;    o += 4096;            // selection scratch, flags, group scan
-    p.bar_off = o;     o += 256;             // mbarriers
+    p.bar_off = o;     o += 512;             // mbarriers
     p.total = o + 1024;
     return p;
 }

@@ -45,6 +45,7 @@ struct KernelShared {
     int seg, nseg;      // decode: segment of the sequence and segments in it
     int pos[kPrefillQT];
     ClusterSmem cs;     // decode: the cluster selection's shared state
+    uint32_t merge_last;   // decode: this cluster merges the sequence's runs (pushed by rank 0)
     SelectSmem sel;
     uint32_t grp[kThreads];   // prefill: group-count scan (first 256 threads)
 };
@@ -167,42 +168,14 @@ __device__ __forceinline__ void prep_queries(const uint8_t* raw, int nrows, uint
     }
 }
 
-// Sequence merge of a multi-segment decode sequence, run by the last CTA of
-// the sequence to finish: the top-k of the segments' sorted runs (`total`
-// composites, zero entries are padding) using the sequence histogram `gh` of
-// the runs' entries; then the per-sequence state is left zeroed for the next
-// call.  Out of line: it runs once per sequence, and keeping its code apart
-// keeps the kernel's common path compact.
-static __device__ __noinline__ void decode_merge(const uint64_t* runs, uint32_t total, uint32_t* gh, uint32_t* ctr,
-                                                 uint32_t* seqflag, uint32_t* seqcnt, uint32_t* hist, uint64_t* buf,
-                                                 int cap, SelectSmem* sel, int k, int32_t* oi, float* os) {
-    const int tid = threadIdx.x;
-    copy_hist_global(hist, gh);
-    const uint32_t flagged = __ldcg(seqflag);
-    __syncthreads();
-    if (flagged) {
-        for (int j = tid; j < k; j += kThreads) {
-            oi[j] = -1;
-            if (os) os[j] = -INFINITY;
-        }
-    } else {
-        // zero entries pad the runs
-        auto each = [&](auto f) { walk_global(runs, total, [&](uint64_t c, bool v) { f(c, v && c != 0ull); }); };
-        auto each_slow = [&](auto f) {
-            walk_global_slow(runs, total, [&](uint64_t c, bool v) { f(c, v && c != 0ull); });
-        };
-        select_topk_from_hist(each, each_slow, hist, k, buf, cap, sel, oi, os);
-    }
-    __syncthreads();
-    reinterpret_cast<uint4*>(gh)[tid] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(gh)[tid + 256] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(gh)[tid + 512] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(gh)[tid + 768] = make_uint4(0, 0, 0, 0);
-    if (tid == 0) {
-        *ctr = 0;
-        *seqflag = 0;
-        *seqcnt = 0;
-    }
+// Clusters a decode sequence of S keys takes: its segments of `cluster`
+// chunks, each chunk the sequence's share of its cluster rounded up to the
+// tile and capped at p.chunk keys; one for an invalid or empty sequence (it
+// writes the -1 outputs).
+__device__ __forceinline__ int decode_clusters_of(int S, const ScoreParams& p, int CL) {
+    if (S <= 0 || S > p.max_seq_len) return 1;
+    const int chunk = min(p.chunk, ((S + CL - 1) / CL + kTileKeys - 1) / kTileKeys * kTileKeys);
+    return (S + CL * chunk - 1) / (CL * chunk);
 }
 
 // Two decode CTAs share an SM only at <= 124 registers per thread (measured
@@ -250,7 +223,10 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
     uint64_t* mdone = bars + 12;           // MMA drain at exit
     uint64_t* qbar = bars + 13;            // query rows staged
     uint64_t* qready = bars + 14;          // decode: every rank's query rows written here
-    uint64_t* cbar = bars + 15;            // decode: [kClBars] cluster barriers of the selection
+    uint64_t* cbar = bars + 15;            // decode: [kClBars] barriers of the segment selection
+    uint64_t* cbar2 = cbar + kClBars;      // decode: [kClBars] barriers of the sequence merge
+    uint64_t* rdone = cbar2 + kClBars;     // decode: every CTA of the cluster wrote its run part
+    uint64_t* rlast = rdone + 1;           // decode: the cluster learnt whether it merges
 
     const int tid = threadIdx.x;
     const int warp = warp_id(), lane = lane_id();
@@ -263,8 +239,54 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
         const int CL = p.cluster;
         const int rank = static_cast<int>(cluster_rank());
         const int cid = blockIdx.x / CL;
-        const int b = cid / p.nseg_max;
-        const int seg = cid - b * p.nseg_max;
+        int b = cid, seg = 0;
+        if (p.nseg_max > 1) {
+            // The grid has nseg_max clusters per sequence; the clusters of the
+            // sequences' real segments take its first ids, sequence by sequence
+            // (an invalid or empty sequence takes one, which writes its -1
+            // outputs), and the rest leave at once without delaying them.
+            const int per = (p.batch + kThreads - 1) / kThreads;
+            int mine = 0;
+            for (int i = 0; i < per; ++i) {
+                const int bb = tid * per + i;
+                if (bb < p.batch) mine += decode_clusters_of(p.seq_lens[bb], p, CL);
+            }
+            int incl = mine;   // inclusive scan over the warp
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) ks->grp[warp] = static_cast<uint32_t>(incl);
+            if (tid == 0) ks->unit_b = -1;
+            __syncthreads();
+            int before = 0, total = 0;
+            for (int w = 0; w < kThreads / 32; ++w) {
+                const int t = static_cast<int>(ks->grp[w]);
+                if (w < warp) before += t;
+                total += t;
+            }
+            const int excl = before + incl - mine;
+            if (cid >= excl && cid < excl + mine) {
+                int acc = excl;
+                for (int i = 0; i < per; ++i) {
+                    const int bb = tid * per + i;
+                    const int nc = decode_clusters_of(p.seq_lens[bb], p, CL);
+                    if (cid < acc + nc) {
+                        ks->unit_b = bb;
+                        ks->seg = cid - acc;
+                        break;
+                    }
+                    acc += nc;
+                }
+            }
+            __syncthreads();
+            (void)total;
+            if (ks->unit_b < 0) return;   // the whole cluster leaves together
+            b = ks->unit_b;
+            seg = ks->seg;
+            __syncthreads();
+        }
         const int S = p.seq_lens[b];
         const bool valid = S >= 0 && S <= p.max_seq_len;
         int chunk = kTileKeys, nseg = 0;
@@ -375,11 +397,16 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
             // each cluster barrier takes one arrive from every CTA
             mbar_init(qready, 1);
             cluster_select_init(cbar);
+            cluster_select_init(cbar2);
+            mbar_init(rdone, kCl);
+            mbar_init(rlast, 1);
         }
         fence_mbar_init();
         if constexpr (kDecode) {
             mbar_arrive_expect_tx(qready, 64 * (kFp8 ? 128 : 256) + 64 * 4);
             cluster_select_expect(cbar);
+            cluster_select_expect(cbar2);
+            mbar_arrive_expect_tx(rlast, 4);
         }
         ks->abort = 0;
         ks->bad = 0;
@@ -644,74 +671,149 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
     } else {
         // ------------------------------------------------ cluster top-k
         // The segment's exact top-k by the whole cluster.  A one-segment
-        // sequence writes its outputs directly; a longer one writes each
-        // segment's sorted top-k (a run of k composites, zero-padded) and the
-        // run's histogram to the workspace, and the last CTA of the sequence
-        // to finish merges the runs.
+        // sequence writes its outputs directly.  A longer one writes each
+        // segment's sorted top-k to the workspace (a run of k composites,
+        // zero-padded); the last cluster of the sequence to finish then merges
+        // the runs with a second selection over them.
         const int b = seq_b;
         const int n = key_end - key_begin;
         const int k = p.topk;
-        const int nround = (n + kThreads - 1) / kThreads * kThreads;
         const bool single = ks->nseg == 1;
+        const uint32_t rank = cluster_rank();
         int32_t* oi = p.out_idx + static_cast<int64_t>(b) * k;
         float* os = p.out_score ? p.out_score + static_cast<int64_t>(b) * k : nullptr;
-        uint64_t* run = p.cand + static_cast<int64_t>(b) * p.cand_cap + static_cast<int64_t>(ks->seg) * k;
-        uint32_t* gh = p.ghist + static_cast<int64_t>(b) * kHistBins;
+        uint64_t* runs_b = p.cand + static_cast<int64_t>(b) * p.cand_cap;
+        uint64_t* run = runs_b + static_cast<int64_t>(ks->seg) * k;
         uint64_t* lists = reinterpret_cast<uint64_t*>(a_tiles);   // 3 x kClCap composites
-        const ClusterBufs B{hist,
-                            reinterpret_cast<uint32_t*>(qtile),
-                            reinterpret_cast<uint32_t*>(lists),
-                            reinterpret_cast<uint32_t*>(lists + kClCap),
-                            lists,
-                            lists + kClCap,
-                            lists + 2 * kClCap,
-                            cbar};
+        ClusterBufs B{hist,
+                      reinterpret_cast<uint32_t*>(qtile),
+                      reinterpret_cast<uint32_t*>(lists),
+                      reinterpret_cast<uint32_t*>(lists + kClCap),
+                      lists,
+                      lists + kClCap,
+                      lists + 2 * kClCap,
+                      cbar};
+        // the chunk's scores as (score key, key index): four scores per load,
+        // two loads in flight per iteration, the same trip count in every lane
+        auto walk_keys = [&](auto f) {
+            const float4* c4 = reinterpret_cast<const float4*>(cscores);
+            const int nj = (n + 3) / 4;
+            const int njr = (nj + kThreads - 1) / kThreads * kThreads;
+#pragma unroll 2
+            for (int j = tid; j < njr; j += kThreads) {
+                const float4 x = j < nj ? c4[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+                const int i = 4 * j;
+                f(score_key(x.x), key_begin + i, i < n);
+                f(score_key(x.y), key_begin + i + 1, i + 1 < n);
+                f(score_key(x.z), key_begin + i + 2, i + 2 < n);
+                f(score_key(x.w), key_begin + i + 3, i + 3 < n);
+            }
+        };
         auto walk = [&](auto f) {
-            for (int i = tid; i < nround; i += kThreads) {
-                const bool v = i < n;
-                f(make_comp(v ? score_key(cscores[i]) : 0u, key_begin + i), v);
+            walk_keys([&](uint32_t key, int idx, bool v) { f(make_comp(key, idx), v); });
+        };
+        auto collect_keys = [&](uint32_t kthr, uint64_t* dst, uint32_t cap, uint64_t* seg, uint32_t* wsum) {
+            return block_collect_keys(walk_keys, kthr, dst, cap, seg, wsum);
+        };
+        auto emit_out = [&](int r, uint64_t c) {
+            oi[r] = comp_index(c);
+            if (os) os[r] = key_score(comp_key(c));
+        };
+        auto pad_out = [&](int count) {
+            for (int j = max(count, 0) + tid; j < k; j += kThreads) {
+                oi[j] = -1;
+                if (os) os[j] = -INFINITY;
             }
         };
-        auto emit = [&](int r, uint64_t c) {
-            if (single) {
-                oi[r] = comp_index(c);
-                if (os) os[r] = key_score(comp_key(c));
-            } else {
-                run[r] = c;
-                atomicAdd(&gh[key_bin(comp_key(c))], 1u);
-            }
-        };
-        const int count = cluster_select(walk, emit, B, k, ks->bad != 0 || ks->abort != 0, &ks->cs, status);
-        const bool first = cluster_rank() == 0;
+        // one selection (one copy of its code) for both cases
+        const int count = cluster_select(
+            walk, collect_keys,
+            [&](int r, uint64_t c) {
+                if (single) emit_out(r, c);
+                else run[r] = c;
+            },
+            B, k, ks->bad != 0 || ks->abort != 0, &ks->cs, status);
         if (single) {
-            if (first) {
-                for (int j = max(count, 0) + tid; j < k; j += kThreads) {
-                    oi[j] = -1;
-                    if (os) os[j] = -INFINITY;
-                }
-            }
+            if (rank == 0) pad_out(count);
             return;
         }
-        if (first) {
+        if (rank == 0) {
             if (count < 0) {
                 if (tid == 0) atomicOr(p.seqflag + b, 1u);
             } else {
                 for (int j = count + tid; j < k; j += kThreads) run[j] = 0ull;
             }
         }
-        // the last CTA of the sequence to finish merges
+        // the cluster's run is written: rank 0 takes the sequence's ticket and
+        // tells every CTA whether this cluster is the last one
         __threadfence();
         __syncthreads();
-        if (tid == 0) ks->ticket = atomicAdd(p.ctr + b, 1u);
-        __syncthreads();
-        if (ks->ticket != static_cast<uint32_t>(ks->nseg * kCl - 1)) return;
+        if (tid == 0) {
+            fence_acq_rel_cluster();
+            mbar_arrive_remote(dsmem_addr(rdone, 0));
+        }
+        if (rank == 0) {
+            if (!mbar_wait_cluster(rdone, 0, status)) ks->abort = 1;
+            if (tid < kCl) {
+                uint32_t last = 0;
+                if (tid == 0) {
+                    __threadfence();
+                    last = (atomicAdd(p.ctr + b, 1u) == static_cast<uint32_t>(ks->nseg - 1)) ? 1u : 0u;
+                }
+                last = __shfl_sync(0xffu, last, 0);
+                dsmem_st_async_u32(dsmem_addr(&ks->merge_last, static_cast<uint32_t>(tid)), last,
+                                   dsmem_addr(rlast, static_cast<uint32_t>(tid)));
+            }
+        }
+        if (!mbar_wait_cluster(rlast, 0, status) || ks->merge_last == 0u) return;
 
-        // ------------------------------------------------ sequence merge (last CTA)
+        // ------------------------------------------------ sequence merge (last cluster)
+        // CTA r takes entries r, r + 8, r + 16, ... of every run, so each CTA
+        // holds about an eighth of the candidates; they are staged in shared
+        // memory where its scores were (zero entries are padding).
         __threadfence();
-        decode_merge(p.cand + static_cast<int64_t>(b) * p.cand_cap,
-                     static_cast<uint32_t>(ks->nseg) * static_cast<uint32_t>(k), gh, p.ctr + b, p.seqflag + b,
-                     p.seqcnt + b, hist, reinterpret_cast<uint64_t*>(a_tiles), kStages * plan.a_stage_bytes / 8,
-                     &ks->sel, k, oi, os);
+        const int nseg = ks->nseg;
+        const int per_run = (k - static_cast<int>(rank) + kCl - 1) / kCl;
+        const int m = nseg * per_run;
+        const int cap_stage = (plan.bid_off - plan.raw_off) / 8;   // the scores region
+        uint64_t* staged = reinterpret_cast<uint64_t*>(cscores);
+        const bool fits = m <= cap_stage;
+        auto run_entry = [&](int i) {
+            const int j = i / per_run;
+            const int e = static_cast<int>(rank) + (i - j * per_run) * kCl;
+            return static_cast<uint64_t>(
+                __ldcg(reinterpret_cast<const unsigned long long*>(runs_b) + static_cast<int64_t>(j) * k + e));
+        };
+        if (fits) {
+#pragma unroll 4
+            for (int i = tid; i < m; i += kThreads) staged[i] = run_entry(i);
+        }
+        const int mround = (m + kThreads - 1) / kThreads * kThreads;
+        auto walk_runs = [&](auto f) {
+            for (int i = tid; i < mround; i += kThreads) {
+                uint64_t c = 0ull;
+                if (i < m) c = fits ? staged[i] : run_entry(i);
+                f(c, c != 0ull);
+            }
+        };
+        for (int i = tid; i < kHistBins; i += kThreads) hist[i] = 0;
+        __syncthreads();
+        walk_runs([&](uint64_t c, bool v) { hist_add_warp(hist, key_bin(comp_key(c)), v); });
+        const uint32_t flagged = __ldcg(p.seqflag + b);
+        B.cbar = cbar2;
+        auto collect_runs = [&](uint32_t kthr, uint64_t* dst, uint32_t cap, uint64_t* seg, uint32_t* wsum) {
+            const uint64_t thr = static_cast<uint64_t>(kthr) << 32;
+            return block_collect_warp(walk_runs, [&](uint64_t c) { return c >= thr; }, dst, cap, seg, wsum);
+        };
+        const int total = cluster_select(walk_runs, collect_runs, emit_out, B, k, flagged != 0u, &ks->cs, status);
+        if (rank == 0) {
+            pad_out(total);
+            if (tid == 0) {
+                p.ctr[b] = 0;
+                p.seqflag[b] = 0;
+                p.seqcnt[b] = 0;
+            }
+        }
     }
 }
 

@@ -116,6 +116,144 @@ __device__ __forceinline__ void warp_append(uint64_t* buf, uint32_t* cnt, uint32
     if (take && pos < cap) buf[pos] = c;
 }
 
+// Block-wide stream compaction without atomics: every composite c of the walk
+// with valid && take(c) goes to dst (the first `cap` of them), thread t's in
+// walk order after those of threads < t.  Two passes over the walk (count,
+// then write at the scanned offset): on sm_103a this measured several times
+// faster than a warp-aggregated atomic append, whose returned offset puts a
+// shared atomic's latency in every iteration.  Returns the number taken
+// (which may exceed cap); wsum: 8 words of scratch.  All 256 threads.
+template <class Walk, class Take>
+__device__ __forceinline__ uint32_t block_collect(Walk walk, Take take, uint64_t* dst, uint32_t cap,
+                                                  uint32_t* wsum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t mine = 0;
+    walk([&](uint64_t c, bool v) { mine += (v && take(c)) ? 1u : 0u; });
+    uint32_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    uint32_t pos = incl - mine, total = 0;
+#pragma unroll
+    for (int w = 0; w < kTopkThreads / 32; ++w) {
+        const uint32_t t = wsum[w];
+        pos += (w < warp) ? t : 0u;
+        total += t;
+    }
+    walk([&](uint64_t c, bool v) {
+        if (v && take(c)) {
+            if (pos < cap) dst[pos] = c;
+            ++pos;
+        }
+    });
+    __syncthreads();
+    return total;
+}
+
+// The same compaction in one pass, for a walk with warp-uniform trip counts:
+// each warp appends its taken composites (ballot + popc, a running count in a
+// register) to its own segment of `seg` (cap / 8 entries per warp), then the
+// segments are copied to dst in warp order.  When a warp's segment overflows,
+// falls back to block_collect.  seg: cap composites of scratch, disjoint
+// from dst.  Returns the number taken.  All 256 threads.
+template <class Walk, class Take>
+__device__ __forceinline__ uint32_t block_collect_warp(Walk walk, Take take, uint64_t* dst, uint32_t cap,
+                                                       uint64_t* seg, uint32_t* wsum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t segcap = cap / (kTopkThreads / 32);
+    uint64_t* mine = seg + warp * segcap;
+    uint32_t cnt = 0;   // the same in every lane
+    walk([&](uint64_t c, bool v) {
+        const bool t = v && take(c);
+        const unsigned m = __ballot_sync(0xffffffffu, t);
+        if (t) {
+            const uint32_t p = cnt + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
+            if (p < segcap) mine[p] = c;
+        }
+        cnt += static_cast<uint32_t>(__popc(m));
+    });
+    if (lane == 0) wsum[warp] = cnt;
+    __syncthreads();
+    uint32_t before = 0, total = 0;
+    bool over = false;
+#pragma unroll
+    for (int w = 0; w < kTopkThreads / 32; ++w) {
+        const uint32_t t = wsum[w];
+        before += (w < warp) ? t : 0u;
+        total += t;
+        over |= t > segcap;
+    }
+    if (!over) {
+        for (uint32_t i = lane; i < cnt; i += 32) dst[before + i] = mine[i];
+    }
+    __syncthreads();
+    if (over) return block_collect(walk, take, dst, cap, wsum);
+    return total;
+}
+
+// block_collect_warp for a walk over 32-bit score keys: walkk(f) calls
+// f(key, index, valid) with warp-uniform trip counts, and the composites of
+// keys >= kthr are collected (the composite is built only for those).  On
+// overflow of a warp's segment, two passes (count, then write at the scanned
+// offset).  Returns the number taken.  All 256 threads.
+template <class WalkK>
+__device__ __forceinline__ uint32_t block_collect_keys(WalkK walkk, uint32_t kthr, uint64_t* dst, uint32_t cap,
+                                                       uint64_t* seg, uint32_t* wsum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t segcap = cap / (kTopkThreads / 32);
+    uint64_t* mine = seg + warp * segcap;
+    uint32_t cnt = 0, own = 0;   // cnt: the warp's (same in every lane); own: this lane's
+    walkk([&](uint32_t key, int idx, bool v) {
+        const bool t = v && key >= kthr;
+        const unsigned m = __ballot_sync(0xffffffffu, t);
+        if (t) {
+            const uint32_t p = cnt + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
+            if (p < segcap) mine[p] = make_comp(key, idx);
+        }
+        cnt += static_cast<uint32_t>(__popc(m));
+        own += t ? 1u : 0u;
+    });
+    if (lane == 0) wsum[warp] = cnt;
+    __syncthreads();
+    uint32_t before = 0, total = 0;
+    bool over = false;
+#pragma unroll
+    for (int w = 0; w < kTopkThreads / 32; ++w) {
+        const uint32_t t = wsum[w];
+        before += (w < warp) ? t : 0u;
+        total += t;
+        over |= t > segcap;
+    }
+    if (!over) {
+        for (uint32_t i = lane; i < cnt; i += 32) dst[before + i] = mine[i];
+        __syncthreads();
+        return total;
+    }
+    // a warp overflowed its segment: thread-ordered write at scanned offsets
+    __syncthreads();
+    uint32_t incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    uint32_t pos = incl - own;
+#pragma unroll
+    for (int w = 0; w < kTopkThreads / 32; ++w) pos += (w < warp) ? wsum[w] : 0u;
+    walkk([&](uint32_t key, int idx, bool v) {
+        if (v && key >= kthr) {
+            if (pos < cap) dst[pos] = make_comp(key, idx);
+            ++pos;
+        }
+    });
+    __syncthreads();
+    return total;
+}
+
 // Candidate walks.  A walk `each(f)` calls f(comp, valid) for every candidate,
 // strided over the block's 256 threads, with the same number of calls in every
 // lane of a warp (lanes past the end get valid = false), so f may use warp
