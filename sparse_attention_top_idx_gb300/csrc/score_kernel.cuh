@@ -608,6 +608,23 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
         if constexpr (kDecode) {
             if (!__all_sync(0xffffffffu, mbar_wait_cluster(qready, 0, status))) ks->abort = 1;   // w'
         }
+        // one query per warp: its 64 head weights stay in registers for the
+        // whole loop, and TMEM is read 16 columns at a time to make room.
+        // (Reloading them per tile made the shared-memory load pipe the
+        // prefill kernel's limit: a broadcast load fills the 32 lanes'
+        // registers at 128 bytes per wavefront, 64 wavefronts per warp-tile.)
+        static_assert(kQPer == 1, "one query per epilogue warp");
+        unsigned long long wr[32];
+        const unsigned long long* wq2 = reinterpret_cast<const unsigned long long*>(wq + j0 * 64);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) wr[i] = wq2[i];
+        int vis_rows = 0, vis_pos = 0;
+        int64_t out_row = 0;
+        if constexpr (!kDecode) {
+            vis_rows = ks->nrows;
+            vis_pos = j0 < vis_rows ? ks->pos[j0] : -1;
+            out_row = static_cast<int64_t>(ks->row0 + j0) * p.score_stride;
+        }
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % kStages;
             const uint32_t ph = static_cast<uint32_t>(t / kStages) & 1u;
@@ -626,18 +643,27 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
             // sum_h w'[h] * max(D[h], 0): even and odd heads in the two lanes of
             // a packed fp32 pair, added at the end
             float res[kQPer];
+            {
+                // heads 0..31: max(D, 0) (ALU pipe); heads 32..63:
+                // D + |D| = 2 max(D, 0) exactly (an add with an absolute-value
+                // operand, FMA pipe), the factor 2 removed at the end (exact)
+                unsigned long long lo = 0ull, hi = 0ull;
 #pragma unroll
-            for (int jj = 0; jj < kQPer; ++jj) {
-                const int j = j0 + jj;
-                unsigned long long acc = 0ull;
-                const unsigned long long* w2 = reinterpret_cast<const unsigned long long*>(wq + j * 64);
-                float v[64];
-                tmem_ld64(lane_base + static_cast<uint32_t>(a * kN + j * 64), v);
+                for (int c = 0; c < 4; ++c) {
+                    float v[16];
+                    tmem_ld16(lane_base + static_cast<uint32_t>(a * kN + j0 * 64 + 16 * c), v);
+                    if (c < 2) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    acc = f2_fma(w2[i], f2_pack(fmaxf(v[2 * i], 0.0f), fmaxf(v[2 * i + 1], 0.0f)), acc);
-                const float2 pr = f2_unpack(acc);
-                res[jj] = kscale * (pr.x + pr.y);
+                        for (int i = 0; i < 8; ++i)
+                            lo = f2_fma(wr[8 * c + i], f2_pack(fmaxf(v[2 * i], 0.0f), fmaxf(v[2 * i + 1], 0.0f)), lo);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            hi = f2_fma(wr[8 * c + i], f2_pack(v[2 * i] + fabsf(v[2 * i]), v[2 * i + 1] + fabsf(v[2 * i + 1])), hi);
+                    }
+                }
+                const float2 pl = f2_unpack(lo), ph2 = f2_unpack(hi);
+                res[0] = kscale * ((pl.x + pl.y) + 0.5f * (ph2.x + ph2.y));
             }
             tc_fence_before();
             __syncwarp();
@@ -649,12 +675,7 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
                 if (valid) cscores[key - key_begin] = res[0];
                 hist_add_warp(hist, key_bin(kk), valid);
             } else {
-#pragma unroll
-                for (int jj = 0; jj < kQPer; ++jj) {
-                    const int j = j0 + jj;
-                    if (j < ks->nrows && key <= ks->pos[j])
-                        p.scores[static_cast<int64_t>(ks->row0 + j) * p.score_stride + key] = res[jj];
-                }
+                if (key <= vis_pos) p.scores[out_row + key] = res[0];
             }
         }
     }
