@@ -280,7 +280,16 @@ __device__ int cluster_select(Walk walk, Collect0 collect0, Emit emit, const Clu
     if (tid < kCl)
         dsmem_st_async_u32(dsmem_addr(&cs->lcnt[rank], static_cast<uint32_t>(tid)), static_cast<uint32_t>(nr),
                            dsmem_addr(&B.cbar[kClBarCount], static_cast<uint32_t>(tid)));
-    block_sort_any(mylist, nr, scratch);
+    if (nr <= 2 * kTopkThreads) {
+        // short list: sort by counting into the scratch buffer, which then
+        // holds the list
+        block_count_sort(mylist, nr, scratch);
+        uint64_t* t = mylist;
+        mylist = scratch;
+        scratch = t;
+    } else {
+        block_sort_any(mylist, nr, scratch);
+    }
     if (!cl_wait(&B.cbar[kClBarCount], status, cs)) return -1;
     int off[kCl + 1];
     off[0] = 0;

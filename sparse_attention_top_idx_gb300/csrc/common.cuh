@@ -190,6 +190,14 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The same barrier in two halves, so that local work can run between them:
+// every thread of every CTA arrives once, then waits.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // Address of the same shared-memory variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
     uint32_t r;

@@ -136,6 +136,43 @@ __device__ __forceinline__ float quant_row_part(const uint8_t* raw_row, int part
     }
 }
 
+// One sixteenth (8 elements, `part` 0..15) of query row r (bf16, staged in
+// shared memory) turned into its B-tile bytes, written to qtile (a tile of
+// `rows` rows): the same encoding as quant_row_part with the 16 lanes of
+// gmask sharing the row (the row's amax reduced over them).  Returns w' of
+// the row (w * sq for fp8, w for bf16).
+template <bool kFp8>
+__device__ __forceinline__ float quant_row_sixteenth(const uint8_t* raw_row, int part, float wv, unsigned gmask,
+                                                     uint8_t* qtile, int r, int rows) {
+    const uint4 v = reinterpret_cast<const uint4*>(raw_row)[part];
+    if constexpr (!kFp8) {
+        *reinterpret_cast<uint4*>(qtile + (part >> 3) * (rows * 128) + sw128_off(r, part & 7)) = v;
+        return wv;
+    } else {
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[2 * e] = __uint_as_float(w4[e] << 16);
+            x[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, o));
+        const float sq = __fdiv_rn(amax, 448.0f);
+        uint32_t c0 = 0, c1 = 0;
+        if (amax != 0.0f) {
+            const DivBy div(sq);
+            c0 = cvt_e4m3x2_pair(div(x[0]), div(x[1])) | (cvt_e4m3x2_pair(div(x[2]), div(x[3])) << 16);
+            c1 = cvt_e4m3x2_pair(div(x[4]), div(x[5])) | (cvt_e4m3x2_pair(div(x[6]), div(x[7])) << 16);
+        }
+        *reinterpret_cast<uint2*>(qtile + sw128_off(r, part >> 1) + (part & 1) * 8) = make_uint2(c0, c1);
+        return wv * sq;
+    }
+}
+
 // Byte offset in the B tile of chunk i (0..3) produced by quant_row_part.
 template <bool kFp8>
 __device__ __forceinline__ int qchunk_off(int r, int part, int i, int rows) {
@@ -381,36 +418,57 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
     const int ntiles = key_end > key_begin ? (key_end - key_begin + kTileKeys - 1) / kTileKeys : 0;
 
     // ------------------------------------------------------------ set-up
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kFp8 ? 1 + kEpiWarps : 1);
+    // Warp 0: lane 0 starts the query rows' load first (decode: this rank's
+    // share of the 64 head rows; prefill: every row) with their head weights,
+    // so its latency overlaps the rest of the set-up; lanes 1..3 initialise
+    // the other barriers in parallel.
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(qbar, 1);
+            fence_mbar_init();
+            const uint64_t pol_q = policy_evict_first();
+            const int r0 = kDecode ? static_cast<int>(cluster_rank()) * (64 / p.cluster) : 0;
+            const int nr = kDecode ? 64 / p.cluster : ks->nrows * 64;
+            const int64_t g0 = static_cast<int64_t>(ks->row0) * 64 + r0;
+            mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(nr) * (kHeadDim * 2 + 4));
+            bulk_load(raw + static_cast<size_t>(r0) * kHeadDim * 2, p.q + g0 * kHeadDim,
+                      static_cast<uint32_t>(nr) * kHeadDim * 2, qbar, pol_q);
+            bulk_load(wq + r0, p.w + g0, static_cast<uint32_t>(nr) * 4, qbar, pol_q);
+            tma_prefetch_desc(&tmap);
+            ks->abort = 0;
+            ks->bad = 0;
+            ks->cs.dead = 0;
+        } else if (lane == 1) {
+            for (int s = 0; s < kStages; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], kFp8 ? 1 + kEpiWarps : 1);
+            }
+            for (int a = 0; a < 2; ++a) {
+                mbar_init(&tfull[a], 1);
+                mbar_init(&tempty[a], kEpiWarps);
+            }
+            mbar_init(mdone, 1);
+            fence_mbar_init();
+        } else if (lane == 2) {
+            if constexpr (kDecode) {
+                // qready completes when the query bytes have arrived
+                // (st.async); the selection's barriers: see cluster_select
+                mbar_init(qready, 1);
+                cluster_select_init(cbar);
+                fence_mbar_init();
+                mbar_arrive_expect_tx(qready, 64 * (kFp8 ? 128 : 256) + 64 * 4);
+                cluster_select_expect(cbar);
+            }
+        } else if (lane == 3) {
+            if constexpr (kDecode) {
+                cluster_select_init(cbar2);
+                mbar_init(rdone, kCl);
+                mbar_init(rlast, 1);
+                fence_mbar_init();
+                cluster_select_expect(cbar2);
+                mbar_arrive_expect_tx(rlast, 4);
+            }
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], kEpiWarps);
-        }
-        mbar_init(mdone, 1);
-        mbar_init(qbar, 1);
-        if constexpr (kDecode) {
-            // qready completes when the query bytes have arrived (st.async);
-            // each cluster barrier takes one arrive from every CTA
-            mbar_init(qready, 1);
-            cluster_select_init(cbar);
-            cluster_select_init(cbar2);
-            mbar_init(rdone, kCl);
-            mbar_init(rlast, 1);
-        }
-        fence_mbar_init();
-        if constexpr (kDecode) {
-            mbar_arrive_expect_tx(qready, 64 * (kFp8 ? 128 : 256) + 64 * 4);
-            cluster_select_expect(cbar);
-            cluster_select_expect(cbar2);
-            mbar_arrive_expect_tx(rlast, 4);
-        }
-        ks->abort = 0;
-        ks->bad = 0;
-        ks->cs.dead = 0;
     }
     if (warp == 1) {
         tmem_alloc(&ks->tmem_base, 2 * kN);
@@ -423,36 +481,35 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
     __syncthreads();
     tc_fence_after();
     // every CTA of the cluster has its barriers and histogram ready before any
-    // CTA touches another's shared memory
-    if constexpr (kDecode) cluster_sync_all();
+    // CTA touches another's shared memory: arrive now, wait after the local
+    // query quantisation below
+    if constexpr (kDecode) cluster_arrive();
     const uint32_t tmem = ks->tmem_base;
 
-    // Warp 0 stages the query rows and starts streaming keys at once.  Decode:
-    // each rank of the cluster quantises 64 / cluster of the 64 head rows
-    // (warp 2) and warps 1..7 send them, as one contiguous run of the 128-byte
-    // swizzled B tile (row r is bytes [128 r, 128 r + 128)) plus the rows'
-    // weights, to every rank as st.async counted on that rank's qready.
-    // Prefill: warps 1..11 build the whole tile and meet on a named barrier.
+    // The query rows are in flight since the set-up; warp 0 starts streaming
+    // keys at once.  Decode: each rank of the cluster quantises 64 / cluster
+    // of the 64 head rows (warp 2) and warps 1..7 send them, as one contiguous
+    // run of the 128-byte swizzled B tile (row r is bytes [128 r, 128 r + 128))
+    // plus the rows' weights, to every rank as st.async counted on that
+    // rank's qready.  Prefill: warps 1..19 build the whole tile and meet on a
+    // named barrier.
     int qrow0 = 0, qrows = 0;
     if constexpr (kDecode) {
         qrows = 64 / p.cluster;
         qrow0 = static_cast<int>(cluster_rank()) * qrows;
-        constexpr int kChunks = kFp8 ? 2 : 4;
+        // 16 threads per row (warps 2 and up) quantise this rank's rows
         const int i = tid - 64;
-        if (i >= 0 && i < qrows * 4) {
-            const int r = qrow0 + (i >> 2), part = i & 3;
-            const unsigned gmask = 0xFu << (threadIdx.x & 28);
+        if (i >= 0 && i < qrows * 16) {
+            const int r = qrow0 + (i >> 4), part = i & 15;
+            const unsigned gmask = 0xFFFFu << (threadIdx.x & 16);
             if (!mbar_wait(qbar, 0, status, &ks->abort)) ks->abort = 1;
-            const float wv = wq[r];
-            uint4 out[4];
-            const float wn = quant_row_part<kFp8>(raw + static_cast<size_t>(r) * 256, part, true, wv, gmask, out);
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-                *reinterpret_cast<uint4*>(qtile + qchunk_off<kFp8>(r, part, c, 64)) = out[c];
+            const float wn = quant_row_sixteenth<kFp8>(raw + static_cast<size_t>(r) * 256, part, wq[r], gmask,
+                                                       qtile, r, 64);
             if (part == 0) wq[r] = wn;
         }
+        __syncthreads();
+        cluster_wait();
         if (warp != 0) {
-            asm volatile("bar.sync 2, %0;" ::"r"(kThreads - 32) : "memory");
             const int run = qrows * 128 / 16;                  // 16-byte chunks per half
             const int per_rank = run * (kFp8 ? 1 : 2) + qrows * 4 / 16;
             for (int j = tid - 32; j < per_rank * p.cluster; j += kThreads - 32) {
@@ -477,22 +534,10 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
 
     // ------------------------------------------------------------ main loop
     if (warp == 0) {
-        // Warp 0: lane 0 stages the query rows and issues the key TMA; the
-        // whole warp prefetches the block ids of up to kBidWindow blocks at a
-        // time into shared memory, so no tile waits on a block-table load.
+        // Warp 0: lane 0 issues the key TMA; the whole warp prefetches the
+        // block ids of up to kBidWindow blocks at a time into shared memory,
+        // so no tile waits on a block-table load.
         int* bids = reinterpret_cast<int*>(smem + plan.bid_off);
-        if (lane == 0) {
-            const uint64_t pol_q = policy_evict_first();
-            // decode: this rank's share of the 64 head rows; prefill: every row
-            const int r0 = kDecode ? qrow0 : 0;
-            const int nr = kDecode ? qrows : ks->nrows * 64;
-            const int64_t g0 = static_cast<int64_t>(ks->row0) * 64 + r0;
-            mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(nr) * (kHeadDim * 2 + 4));
-            bulk_load(raw + static_cast<size_t>(r0) * kHeadDim * 2, p.q + g0 * kHeadDim,
-                      static_cast<uint32_t>(nr) * kHeadDim * 2, qbar, pol_q);
-            bulk_load(wq + r0, p.w + g0, static_cast<uint32_t>(nr) * 4, qbar, pol_q);
-            tma_prefetch_desc(&tmap);
-        }
         const uint64_t pol = kDecode ? policy_evict_first() : policy_evict_last();
         const int lb_end = (key_end + kBs - 1) / kBs;
         int lb_lo = 0, lb_hi = 0;          // window of prefetched logical blocks

@@ -587,6 +587,49 @@ __device__ __forceinline__ void block_sort_desc_r(uint64_t* a, int n, uint64_t* 
     else block_rank_sort<kMaxE>(a, n, runs);
 }
 
+// Sort by counting, for short lists: the position of a[i] is the number of
+// larger entries (composites are unique), found by comparing it with every
+// entry (shared-memory broadcasts, four independent counts per thread for
+// overlap); then each entry is written to its position in out.  Warps that
+// hold no entry skip the comparisons.  n <= 512, all 256 threads; out must
+// not overlap a.
+__device__ __forceinline__ void block_count_sort(const uint64_t* a, int n, uint64_t* out) {
+    const int t = threadIdx.x;
+    if (t - (t & 31) < n) {
+        const uint64_t x0 = t < n ? a[t] : 0ull;
+        if (n <= kTopkThreads) {
+            int c0 = 0, c1 = 0, c2 = 0, c3 = 0, j = 0;
+#pragma unroll 1
+            for (; j + 3 < n; j += 4) {
+                c0 += a[j] > x0;
+                c1 += a[j + 1] > x0;
+                c2 += a[j + 2] > x0;
+                c3 += a[j + 3] > x0;
+            }
+            for (; j < n; ++j) c0 += a[j] > x0;
+            if (t < n) out[c0 + c1 + c2 + c3] = x0;
+        } else {
+            const uint64_t x1 = t + kTopkThreads < n ? a[t + kTopkThreads] : 0ull;
+            int c0 = 0, c1 = 0, d0 = 0, d1 = 0, j = 0;
+#pragma unroll 1
+            for (; j + 1 < n; j += 2) {
+                const uint64_t y0 = a[j], y1 = a[j + 1];
+                c0 += y0 > x0;
+                c1 += y1 > x0;
+                d0 += y0 > x1;
+                d1 += y1 > x1;
+            }
+            if (j < n) {
+                c0 += a[j] > x0;
+                d0 += a[j] > x1;
+            }
+            if (t < n) out[c0 + c1] = x0;
+            if (t + kTopkThreads < n) out[d0 + d1] = x1;
+        }
+    }
+    __syncthreads();
+}
+
 // One out-of-line copy per kernel: the kernels sort from several places, each
 // once per block and from a cold instruction cache, so sharing one copy keeps
 // their code (and the instruction fetches) small.
