@@ -44,10 +44,9 @@ N_POOL_COPIES = 9
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources they were taken on; a stale hash reports null.
 NCU_TRAFFIC = {
-    # profiles/score_kernel_decode_b32_s4500_10000_top512.md
-    ("decode", "cecde544ac6be281"): 31553280,
-    # profiles/score_kernel_prefill_s22000_t8192_top1024.md (scoring kernel)
-    ("prefill", "cecde544ac6be281"): 139460096 + 528051456,
+    ("decode", "9c1f86a54ca594b2"): 31451136 + 0,
+    ("longctx", "9c1f86a54ca594b2"): 277262592 + 3018752,
+    ("prefill", "9c1f86a54ca594b2"): 139463168 + 531216896,   # the scoring kernel
 }
 
 
