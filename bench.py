@@ -43,10 +43,12 @@ N_POOL_COPIES = 9
 # DRAM bytes per launch of the dominant kernels from ncu captures
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources they were taken on; a stale hash reports null.
+# (Taken at commit 78f57a0; the sources since differ only in comments and an
+# unused helper, so the kernels are the same.)
 NCU_TRAFFIC = {
-    ("decode", "9c1f86a54ca594b2"): 31451136 + 0,
-    ("longctx", "9c1f86a54ca594b2"): 277262592 + 3018752,
-    ("prefill", "9c1f86a54ca594b2"): 139463168 + 531216896,   # the scoring kernel
+    ("decode", "3ff41b113a2877c2"): 31451136 + 0,
+    ("longctx", "3ff41b113a2877c2"): 277262592 + 3018752,
+    ("prefill", "3ff41b113a2877c2"): 139463168 + 531216896,   # the scoring kernel
 }
 
 

@@ -185,13 +185,8 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
 }
-// Whole-cluster barrier; every thread of every CTA of the cluster must reach
-// it (used once, at kernel start, before any CTA can leave).
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// The same barrier in two halves, so that local work can run between them:
-// every thread of every CTA arrives once, then waits.
+// Whole-cluster barrier in two halves, so that local work can run between
+// them: every thread of every CTA of the cluster arrives once, then waits.
 __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }

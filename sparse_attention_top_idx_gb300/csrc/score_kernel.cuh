@@ -7,13 +7,14 @@
 // verbatim lines" (ROCm/ATOM issue #1507, section "How it was isolated") read
 // it: straight from the paged blocks through the block table.
 //
-// One CTA of 256 threads (8 warps) per work unit:
-//   decode  (kQT = 1): a chunk of one sequence's keys against its 64 query
-//                      heads (N = 64); the CTAs of a sequence segment form a
-//                      thread-block cluster that selects the top-k together;
-//   prefill (kQT = 4): up to 4 consecutive query rows of one sequence against
-//                      every key they can see (N = 256); scores go to the
-//                      workspace for the row select kernel.
+// Work units:
+//   decode  (kQT = 1, 256 threads): a chunk of one sequence's keys against
+//                      its 64 query heads (N = 64); the 8 CTAs of a sequence
+//                      segment form a thread-block cluster that selects the
+//                      top-k together (cluster_select.cuh);
+//   prefill (kQT = 4, 640 threads): up to 4 consecutive query rows of one
+//                      sequence against every key they can see (N = 256);
+//                      scores go to the workspace for the row select kernel.
 // The contraction D[s, (t, h)] = sum_d k[s, d] q[t, h, d] runs on the 5th-gen
 // tensor cores: M = 128 keys (A, K-major, TMA-loaded 64- or 32-row boxes of the
 // paged blocks, 128-byte swizzle), N = 64 * kQT query-heads (B, quantised by
@@ -21,10 +22,12 @@
 // (two buffers so the epilogue of tile i overlaps the MMA of tile i + 1).
 // fp8 keys use kind::f8f6f4 (e4m3 x e4m3), bf16 keys kind::f16.
 //
-// Warp roles: warp 0 lane 0 issues the bulk copy of the query rows and then
-// the key TMA; warps 1..7 quantise the queries into the B tile; warp 1 owns
-// TMEM and its lane 0 issues the MMAs; warps 4..7 (TMEM lane quadrants 0..3,
-// one key row per thread) run the epilogue ks[s] * sum_h w'[t, h] * max(D, 0).
+// Warp roles: warp 0 lane 0 starts the query rows' bulk copy, then issues the
+// key TMA (the warp prefetches block ids); the other warps quantise the
+// queries into the B tile; warp 1 owns TMEM and its lane 0 issues the MMAs;
+// warps 4.. (decode 4, prefill 16: one per TMEM lane quadrant and query, one
+// key row per thread) run the epilogue ks[s] * sum_h w'[t, h] * max(D, 0)
+// with the query's head weights held in registers.
 #pragma once
 
 #include <cuda_bf16.h>
