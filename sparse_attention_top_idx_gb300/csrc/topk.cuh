@@ -290,10 +290,11 @@ __device__ __forceinline__ void walk_global(const uint64_t* a, uint32_t n, F f) 
 }
 
 // A global row of n fp32 scores (16-byte aligned, readable up to n rounded up
-// to 4): candidate i is (score_key(row[i]), i).  Eight float4 loads in flight.
+// to 4): candidate i is (score_key(row[i]), i).  Four float4 loads in flight
+// (measured best: eight or sixteen made the select slower, two no faster).
 template <class F>
 __device__ __forceinline__ void walk_row(const float* row, int n, F f) {
-    constexpr int U = 8;
+    constexpr int U = 4;
     const float4* r4 = reinterpret_cast<const float4*>(row);
     for (int b0 = 0; b0 < n; b0 += kTopkThreads * 4 * U) {
         float4 v[U];
