@@ -692,26 +692,24 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
             // a packed fp32 pair, added at the end
             float res[kQPer];
             {
-                // heads 0..31: max(D, 0) (ALU pipe); heads 32..63:
-                // D + |D| = 2 max(D, 0) exactly (an add with an absolute-value
-                // operand, FMA pipe), the factor 2 removed at the end (exact)
-                unsigned long long lo = 0ull, hi = 0ull;
+                // max(D, 0) as D + |D| = 2 max(D, 0) exactly: an add with an
+                // absolute-value operand on the FMA pipe (the ALU pipe, where
+                // a max goes, was the epilogue's busiest; moving all 64 there
+                // measured fastest, and one accumulator chain faster than
+                // two), the factor 2 removed at the end (exact); 16 heads
+                // per TMEM load
+                unsigned long long acc = 0ull;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     float v[16];
                     tmem_ld16(lane_base + static_cast<uint32_t>(a * kN + j0 * 64 + 16 * c), v);
-                    if (c < 2) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            lo = f2_fma(wr[8 * c + i], f2_pack(fmaxf(v[2 * i], 0.0f), fmaxf(v[2 * i + 1], 0.0f)), lo);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            hi = f2_fma(wr[8 * c + i], f2_pack(v[2 * i] + fabsf(v[2 * i]), v[2 * i + 1] + fabsf(v[2 * i + 1])), hi);
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        acc = f2_fma(wr[8 * c + i],
+                                     f2_pack(v[2 * i] + fabsf(v[2 * i]), v[2 * i + 1] + fabsf(v[2 * i + 1])), acc);
                 }
-                const float2 pl = f2_unpack(lo), ph2 = f2_unpack(hi);
-                res[0] = kscale * ((pl.x + pl.y) + 0.5f * (ph2.x + ph2.y));
+                const float2 pr = f2_unpack(acc);
+                res[0] = kscale * (0.5f * (pr.x + pr.y));
             }
             tc_fence_before();
             __syncwarp();
