@@ -96,6 +96,40 @@ def test_ties_go_to_lower_index(mode):
     check(W2, mode, got2)
 
 
+@pytest.mark.parametrize("k", [512, 2048])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_multisegment_ties(mode, k):
+    # every key identical in a sequence of two segments: each CTA's whole
+    # chunk is candidates (fp8: more than a CTA's candidate list holds), the
+    # refinement runs through the index bits, and for k = 2048 the merge of
+    # the tied runs refines as well; the top-k is the first k positions
+    S = 70000 if mode == 0 else 20000
+    W = wl.make_workload("mties", [S, 3000], [1, 1], topk=k, seed=41 + mode)
+    for b in range(W.batch):
+        W.keys[b][:] = W.keys[b][0]
+    got = run_decode(W, mode)
+    assert np.array_equal(got["idx"][0], np.arange(k))
+    assert np.array_equal(got["idx"][1], np.arange(k))
+    assert np.all(got["score"][0] == got["score"][0][0])
+
+
+def test_topk_2048_one_and_two_segments():
+    # the largest k over a one-segment and a two-segment sequence
+    W = wl.make_workload("k2048", [20000, 70000], [1, 1], topk=2048, seed=43)
+    got = run_decode(W, dsaidx.FP8)
+    check(W, dsaidx.FP8, got)
+
+
+def test_bf16_many_segments_merge_reads_runs_from_memory():
+    # bf16 chunks hold at most 2048 keys, so 300000 keys take 19 segments;
+    # with k = 1024 a merging CTA's share of the runs exceeds the shared
+    # staging area and the merge reads the runs from global memory
+    W = wl.make_workload("bf16long", [300000, 5000], [1, 1], topk=1024, seed=44)
+    got = run_decode(W, dsaidx.BF16)
+    check(W, dsaidx.BF16, got)
+    assert got["idx"][0][0] == W.needle_pos[0]
+
+
 def test_deterministic_and_workspace_reuse():
     W = wl.make_workload("det", [4500, 10000, 300, 7777], [1] * 4, topk=512, seed=8)
     outs = run_decode(W, dsaidx.FP8, reps=5)
