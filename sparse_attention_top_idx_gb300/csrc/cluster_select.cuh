@@ -8,13 +8,15 @@
 //
 // Every CTA holds the composites of its own chunk of keys and a 4096-bin
 // histogram of their top 12 bits.  A remote shared-memory load costs a round
-// trip of ~0.3 us on GB300 and a cluster barrier more, so after one barrier
-// (every histogram complete) data only moves by one-way pushes (st.async,
-// counted on the receiver's mbarrier):
-//   1. every CTA sums one 512-bin slice of the histogram over the cluster
-//      (eight remote 8-byte loads per thread) and pushes the sum, with its
-//      device-check flag, to every CTA: each CTA then holds the cluster's
-//      histogram and finds the bin of the k-th largest composite by itself;
+// trip of ~0.3 us on GB300 and a cluster barrier more, so data moves by
+// one-way pushes (st.async, counted on the receiver's mbarrier):
+//   1. every CTA sums one 512-bin slice of the histogram over the cluster --
+//      with a receive area (small chunks), every CTA pushes each owner its
+//      slice at the end of its key loop; otherwise after one cluster barrier
+//      each CTA pulls its slice from every CTA (eight remote 8-byte loads per
+//      thread) -- and pushes the sum, with its device-check flag, to every
+//      CTA: each CTA then holds the cluster's histogram and finds the bin of
+//      the k-th largest composite by itself;
 //      when the bins at or above it hold more than kClCap composites (a wide
 //      boundary bin, or ties), 256-bin histograms of the next 8 bits of the
 //      boundary group, pushed the same way, refine the threshold a level at a
@@ -25,8 +27,10 @@
 //   3. every CTA ranks each of its candidates by binary searches in the other
 //      CTAs' lists; rank r < k goes to output position r.
 // Every push into a CTA is awaited by that CTA, and every remote load of a
-// CTA's histogram happens before the loader's first push, so no CTA leaves
-// while another still reads or writes its shared memory.
+// CTA's histogram happens before the loader's first push of the summed
+// slice, so no CTA leaves while another still reads or writes its shared
+// memory.  The pushes of step 1 land in areas a CTA does not use during its
+// key loop (the receive area) or after every CTA has left it (the rest).
 #pragma once
 
 #include "common.cuh"
@@ -43,10 +47,12 @@ constexpr int kClBarFull = 1;                   // the summed histogram and the 
 constexpr int kClBarRefine0 = 2;                // level l's sub-histograms have arrived: 2 + l
 constexpr int kClBarCount = kClBarRefine0 + kClLevels;   // every CTA's candidate count has arrived
 constexpr int kClBarList = kClBarCount + 1;     // every CTA's sorted candidates have arrived
-constexpr int kClBars = kClBarList + 1;
+constexpr int kClBarRecv = kClBarList + 1;      // every CTA's slice of this CTA's bins has arrived
+constexpr int kClBars = kClBarRecv + 1;
 constexpr uint32_t kClFullBytes = kHistBins * 4 + kCl * 4;
 constexpr uint32_t kClSubBytes = kCl * 256 * 4;
 constexpr uint32_t kClCountBytes = kCl * 4;
+constexpr uint32_t kClRecvBytes = kCl * kClSliceBins * 4;
 static_assert(kClCap >= IDX_MAX_TOPK, "a cluster must be able to rank k candidates");
 static_assert(kClSliceBins == 2 * 256, "each of 256 threads sums two bins");
 
@@ -73,6 +79,7 @@ struct ClusterBufs {
     uint64_t* gath;   // [kClCap] every CTA's sorted list, in rank order (received)
     uint64_t* runs;   // [kClCap] sort scratch
     uint64_t* cbar;   // [kClBars] barriers of the selection
+    uint32_t* recv;   // [kCl][512] every CTA's slice of this CTA's bins (received), or null
 };
 
 // Barrier set-up, by one thread before the cluster's first barrier: the
@@ -87,6 +94,7 @@ __device__ __forceinline__ void cluster_select_expect(uint64_t* cbar) {
     mbar_arrive_expect_tx(&cbar[kClBarFull], kClFullBytes);
     for (int l = 0; l < kClLevels; ++l) mbar_arrive_expect_tx(&cbar[kClBarRefine0 + l], kClSubBytes);
     mbar_arrive_expect_tx(&cbar[kClBarCount], kClCountBytes);
+    mbar_arrive_expect_tx(&cbar[kClBarRecv], kClRecvBytes);
 }
 
 __device__ __forceinline__ bool cl_wait(uint64_t* bar, int32_t* status, ClusterSmem* cs) {
@@ -165,33 +173,53 @@ __device__ int cluster_select(Walk walk, Collect0 collect0, Emit emit, const Clu
     const int tid = threadIdx.x;
     const uint32_t rank = cluster_rank();
 
-    // every CTA's histogram is complete (and its key stage buffers are free)
-    __syncthreads();
-    if (tid < kCl) {
-        fence_acq_rel_cluster();
-        mbar_arrive_remote(dsmem_addr(&B.cbar[kClBarHist], static_cast<uint32_t>(tid)));
-    }
-    if (!cl_wait(&B.cbar[kClBarHist], status, cs)) return -1;
-
-    // (1) sum this CTA's 512-bin slice over the cluster, push it to every CTA
-    {
-        const uint32_t off = (static_cast<uint32_t>(kClSliceBins) * rank + 2u * static_cast<uint32_t>(tid)) * 4u;
+    // (1) the cluster's histogram, summed slice by slice: CTA r sums bins
+    //     [512 r, 512 r + 512) and pushes the sum, with its flag, to every CTA
+    uint32_t a0 = 0, a1 = 0;
+    const uint32_t soff = (static_cast<uint32_t>(kClSliceBins) * rank + 2u * static_cast<uint32_t>(tid)) * 4u;
+    if (B.recv) {
+        // one-way: every CTA pushes each owner its slice of that owner's bins
+        // as soon as its own histogram is complete (the receive area is not
+        // used before); the owner waits for all eight and adds them up
+        __syncthreads();
+        for (int c = tid; c < kCl * (kClSliceBins / 4); c += kTopkThreads) {
+            const uint32_t q = static_cast<uint32_t>(c / (kClSliceBins / 4));
+            const int j = c - static_cast<int>(q) * (kClSliceBins / 4);
+            const uint4 v = reinterpret_cast<const uint4*>(B.hist + q * kClSliceBins)[j];
+            dsmem_st_async_v4(dsmem_addr(B.recv + rank * kClSliceBins + 4 * j, q), v,
+                              dsmem_addr(&B.cbar[kClBarRecv], q));
+        }
+        if (!cl_wait(&B.cbar[kClBarRecv], status, cs)) return -1;
+#pragma unroll
+        for (int q = 0; q < kCl; ++q) {
+            const uint2 h = reinterpret_cast<const uint2*>(B.recv + q * kClSliceBins)[tid];
+            a0 += h.x;
+            a1 += h.y;
+        }
+    } else {
+        // every CTA's histogram is complete (and its key stage buffers are
+        // free): one barrier, then each CTA pulls its bins from every CTA
+        __syncthreads();
+        if (tid < kCl) {
+            fence_acq_rel_cluster();
+            mbar_arrive_remote(dsmem_addr(&B.cbar[kClBarHist], static_cast<uint32_t>(tid)));
+        }
+        if (!cl_wait(&B.cbar[kClBarHist], status, cs)) return -1;
         uint2 h[kCl];
 #pragma unroll
-        for (int q = 0; q < kCl; ++q) h[q] = dsmem_ld_v2(dsmem_addr(B.hist, q) + off);
-        uint32_t a0 = 0, a1 = 0;
+        for (int q = 0; q < kCl; ++q) h[q] = dsmem_ld_v2(dsmem_addr(B.hist, q) + soff);
 #pragma unroll
         for (int q = 0; q < kCl; ++q) {
             a0 += h[q].x;
             a1 += h[q].y;
         }
-#pragma unroll
-        for (int q = 0; q < kCl; ++q)
-            dsmem_st_async_v2(dsmem_addr(B.full, q) + off, a0, a1, dsmem_addr(&B.cbar[kClBarFull], q));
-        if (tid < kCl)
-            dsmem_st_async_u32(dsmem_addr(&cs->flag[rank], static_cast<uint32_t>(tid)), flagged ? 1u : 0u,
-                               dsmem_addr(&B.cbar[kClBarFull], static_cast<uint32_t>(tid)));
     }
+#pragma unroll
+    for (int q = 0; q < kCl; ++q)
+        dsmem_st_async_v2(dsmem_addr(B.full, q) + soff, a0, a1, dsmem_addr(&B.cbar[kClBarFull], q));
+    if (tid < kCl)
+        dsmem_st_async_u32(dsmem_addr(&cs->flag[rank], static_cast<uint32_t>(tid)), flagged ? 1u : 0u,
+                           dsmem_addr(&B.cbar[kClBarFull], static_cast<uint32_t>(tid)));
     if (!cl_wait(&B.cbar[kClBarFull], status, cs)) return -1;
     uint32_t anyflag = 0;
 #pragma unroll

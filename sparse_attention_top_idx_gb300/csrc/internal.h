@@ -67,23 +67,26 @@ struct ScoreParams {
 // Shared-memory plan of the scoring kernel for (fp8, queries per CTA, chunk).
 struct SmemPlan {
     int stages, a_stage_bytes, q_bytes, n_cols;
-    int a_off, q_off, scale_off, w_off, hist_off, raw_off, bid_off, misc_off, bar_off;
+    int a_off, recv_off, recv_bytes, q_off, scale_off, w_off, hist_off, raw_off, bid_off, misc_off, bar_off;
     int total;   // bytes to request (includes 1 KB of alignment slack)
 };
 
-// Decode keeps two CTAs per SM (<= ~111 KB each for fp8 keys): four key stages
-// while the chunk's scores take <= 16 KB, three for larger chunks.  The raw
-// query rows are staged where the decode scores later go (or, for prefill,
-// in a 64 KB region of their own).
+// Decode keeps two CTAs per SM (<= ~112 KB each for fp8 keys): while the
+// chunk's scores take <= 16 KB, three key stages and a 16 KB area that
+// receives the other CTAs' histogram slices at the end (cluster_select);
+// three stages for larger chunks.  The raw query rows are staged where the
+// decode scores later go (or, for prefill, in a 64 KB region of their own).
 __host__ __device__ inline SmemPlan make_plan(bool fp8, int qt, int chunk) {
     SmemPlan p{};
     p.n_cols = 64 * qt;
-    p.stages = (qt == 1) ? (fp8 ? (chunk <= 4096 ? 4 : 3) : 2) : (fp8 ? 4 : 2);
+    p.stages = (qt == 1) ? (fp8 ? 3 : 2) : (fp8 ? 4 : 2);
+    p.recv_bytes = (qt == 1 && fp8 && chunk <= 4096) ? 16384 : 0;
     p.a_stage_bytes = fp8 ? 16384 : 32768;
     p.q_bytes = p.n_cols * (fp8 ? 128 : 256);
     const int raw_bytes = (qt == 1) ? (chunk * 4 > 16384 ? chunk * 4 : 16384) : qt * 16384;
     int o = 0;
     p.a_off = o;       o += p.stages * p.a_stage_bytes;
+    p.recv_off = o;    o += p.recv_bytes;
     p.q_off = o;       o += p.q_bytes;
     p.scale_off = o;   o += fp8 ? p.stages * 512 : 0;
     p.w_off = o;       o += p.n_cols * 4;

@@ -759,7 +759,8 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
                       lists,
                       lists + kClCap,
                       lists + 2 * kClCap,
-                      cbar};
+                      cbar,
+                      plan.recv_bytes ? reinterpret_cast<uint32_t*>(smem + plan.recv_off) : nullptr};
         // the chunk's scores as (score key, key index): four scores per load,
         // two loads in flight per iteration, the same trip count in every lane
         auto walk_keys = [&](auto f) {
