@@ -43,12 +43,10 @@ N_POOL_COPIES = 9
 # DRAM bytes per launch of the dominant kernels from ncu captures
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources they were taken on; a stale hash reports null.
-# (Taken at commit 78f57a0; the sources since differ only in comments and an
-# unused helper, so the kernels are the same.)
 NCU_TRAFFIC = {
-    ("decode", "3ff41b113a2877c2"): 31451136 + 0,
-    ("longctx", "3ff41b113a2877c2"): 277262592 + 3018752,
-    ("prefill", "3ff41b113a2877c2"): 139463168 + 531216896,   # the scoring kernel
+    ("decode", "02c9d96ab9142728"): 31450624 + 0,
+    ("longctx", "02c9d96ab9142728"): 277265664 + 3192320,
+    ("prefill", "02c9d96ab9142728"): 139508224 + 528729856,   # the scoring kernel
 }
 
 
