@@ -130,6 +130,20 @@ def test_bf16_many_segments_merge_reads_runs_from_memory():
     assert got["idx"][0][0] == W.needle_pos[0]
 
 
+def test_many_sequences_and_a_one_key_segment():
+    # 300 sequences (the grid's cluster ids come from a scan over more than
+    # one sequence per thread), one of 65537 keys whose second segment holds a
+    # single key (its run is one entry and padding), one empty, and k larger
+    # than the short sequences
+    lens = [90 + (7 * i) % 50 for i in range(300)]
+    lens[17] = 65537
+    lens[200] = 0
+    W = wl.make_workload("many", lens, [1] * 300, topk=256, seed=45)
+    got = run_decode(W, dsaidx.FP8)
+    check(W, dsaidx.FP8, got, rows=[0, 17, 99, 199, 201, 299])
+    assert np.all(got["idx"][200] == -1)
+
+
 def test_deterministic_and_workspace_reuse():
     W = wl.make_workload("det", [4500, 10000, 300, 7777], [1] * 4, topk=512, seed=8)
     outs = run_decode(W, dsaidx.FP8, reps=5)
