@@ -49,6 +49,7 @@ constexpr int kClBarCount = kClBarRefine0 + kClLevels;   // every CTA's candidat
 constexpr int kClBarList = kClBarCount + 1;     // every CTA's sorted candidates have arrived
 constexpr int kClBarRecv = kClBarList + 1;      // every CTA's slice of this CTA's bins has arrived
 constexpr int kClBars = kClBarRecv + 1;
+constexpr int kCountSortMax = 96;   // longest candidate list sorted by counting
 constexpr uint32_t kClFullBytes = kHistBins * 4 + kCl * 4;
 constexpr uint32_t kClSubBytes = kCl * 256 * 4;
 constexpr uint32_t kClCountBytes = kCl * 4;
@@ -308,9 +309,10 @@ __device__ int cluster_select(Walk walk, Collect0 collect0, Emit emit, const Clu
     if (tid < kCl)
         dsmem_st_async_u32(dsmem_addr(&cs->lcnt[rank], static_cast<uint32_t>(tid)), static_cast<uint32_t>(nr),
                            dsmem_addr(&B.cbar[kClBarCount], static_cast<uint32_t>(tid)));
-    if (nr <= 2 * kTopkThreads) {
+    if (nr <= kCountSortMax) {
         // short list: sort by counting into the scratch buffer, which then
-        // holds the list
+        // holds the list (its cost grows with the square of the length: the
+        // warp-run sort is faster above about a hundred entries)
         block_count_sort(mylist, nr, scratch);
         uint64_t* t = mylist;
         mylist = scratch;

@@ -510,9 +510,12 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
                                                        qtile, r, 64);
             if (part == 0) wq[r] = wn;
         }
-        __syncthreads();
-        cluster_wait();
+        // warps 1.. meet on a named barrier and then on the cluster barrier;
+        // warp 0 goes straight to the key loads (they touch only this CTA's
+        // shared memory) and waits on the cluster barrier after its loop
         if (warp != 0) {
+            asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");
+            cluster_wait();
             const int run = qrows * 128 / 16;                  // 16-byte chunks per half
             const int per_rank = run * (kFp8 ? 1 : 2) + qrows * 4 / 16;
             for (int j = tid - 32; j < per_rank * p.cluster; j += kThreads - 32) {
@@ -606,6 +609,8 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
                 mbar_wait(&full[u % kStages], static_cast<uint32_t>(u / kStages) & 1u, status, nullptr);
             mbar_wait(qbar, 0, status, nullptr);
         }
+        __syncwarp();
+        if constexpr (kDecode) cluster_wait();
     } else if (warp == 1 && lane == 0) {
         // MMA issuer
         constexpr uint32_t idesc = idesc_make(kFp8, kTileKeys, kN);

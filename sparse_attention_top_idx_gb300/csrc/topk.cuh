@@ -589,43 +589,44 @@ __device__ __forceinline__ void block_sort_desc_r(uint64_t* a, int n, uint64_t* 
 }
 
 // Sort by counting, for short lists: the position of a[i] is the number of
-// larger entries (composites are unique), found by comparing it with every
-// entry (shared-memory broadcasts, four independent counts per thread for
-// overlap); then each entry is written to its position in out.  Warps that
-// hold no entry skip the comparisons.  n <= 512, all 256 threads; out must
+// larger entries (composites are unique).  P = 1, 2, 4 or 8 consecutive
+// threads share an entry (the most that fit in the block): each compares it
+// with its contiguous part of the list, two entries per 16-byte shared-memory
+// load and eight per step into independent counts, and the P counts are added
+// with shuffles.  Warps that hold no entry skip the comparisons.  n <= 256,
+// all 256 threads; a 16-byte aligned with room for n + 1 entries; out must
 // not overlap a.
 __device__ __forceinline__ void block_count_sort(const uint64_t* a, int n, uint64_t* out) {
     const int t = threadIdx.x;
-    if (t - (t & 31) < n) {
-        const uint64_t x0 = t < n ? a[t] : 0ull;
-        if (n <= kTopkThreads) {
-            int c0 = 0, c1 = 0, c2 = 0, c3 = 0, j = 0;
+    {
+        int lp = 0;   // log2 of the threads per entry
+        while (lp < 3 && (n << (lp + 1)) <= kTopkThreads) ++lp;
+        const int e = t >> lp, part = t & ((1 << lp) - 1);
+        if (((t & ~31) >> lp) < n) {
+            const uint64_t x = e < n ? a[e] : 0ull;
+            const int len = (((n + (1 << lp) - 1) >> lp) + 1) & ~1;   // even: aligned pairs
+            const int j1 = min(n, part * len + len);
+            const uint4* a4 = reinterpret_cast<const uint4*>(a);
+            int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
 #pragma unroll 1
-            for (; j + 3 < n; j += 4) {
-                c0 += a[j] > x0;
-                c1 += a[j + 1] > x0;
-                c2 += a[j + 2] > x0;
-                c3 += a[j + 3] > x0;
+            for (int j = part * len; j < j1; j += 8) {
+                uint64_t y[8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int jj = j + 2 * u;
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (jj < j1) v = a4[jj >> 1];
+                    y[2 * u] = (static_cast<uint64_t>(v.y) << 32) | v.x;
+                    y[2 * u + 1] = jj + 1 < j1 ? ((static_cast<uint64_t>(v.w) << 32) | v.z) : 0ull;
+                }
+                c0 += (y[0] > x) + (y[4] > x);
+                c1 += (y[1] > x) + (y[5] > x);
+                c2 += (y[2] > x) + (y[6] > x);
+                c3 += (y[3] > x) + (y[7] > x);
             }
-            for (; j < n; ++j) c0 += a[j] > x0;
-            if (t < n) out[c0 + c1 + c2 + c3] = x0;
-        } else {
-            const uint64_t x1 = t + kTopkThreads < n ? a[t + kTopkThreads] : 0ull;
-            int c0 = 0, c1 = 0, d0 = 0, d1 = 0, j = 0;
-#pragma unroll 1
-            for (; j + 1 < n; j += 2) {
-                const uint64_t y0 = a[j], y1 = a[j + 1];
-                c0 += y0 > x0;
-                c1 += y1 > x0;
-                d0 += y0 > x1;
-                d1 += y1 > x1;
-            }
-            if (j < n) {
-                c0 += a[j] > x0;
-                d0 += a[j] > x1;
-            }
-            if (t < n) out[c0 + c1] = x0;
-            if (t + kTopkThreads < n) out[d0 + d1] = x1;
+            int c = c0 + c1 + c2 + c3;
+            for (int o = 1; o < (1 << lp); o <<= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+            if (part == 0 && e < n) out[c] = x;
         }
     }
     __syncthreads();
