@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
     uint64_t* cbar2 = cbar + kClBars;      // decode: [kClBars] barriers of the sequence merge
     uint64_t* rdone = cbar2 + kClBars;     // decode: every CTA of the cluster wrote its run part
     uint64_t* rlast = rdone + 1;           // decode: the cluster learnt whether it merges
+    uint64_t* bready = rlast + 1;          // decode: the chunk's block ids are in shared memory
 
     const int tid = threadIdx.x;
     const int warp = warp_id(), lane = lane_id();
@@ -467,6 +468,7 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
                 cluster_select_init(cbar2);
                 mbar_init(rdone, kCl);
                 mbar_init(rlast, 1);
+                mbar_init(bready, 1);
                 fence_mbar_init();
                 cluster_select_expect(cbar2);
                 mbar_arrive_expect_tx(rlast, 4);
@@ -489,20 +491,19 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
     if constexpr (kDecode) cluster_arrive();
     const uint32_t tmem = ks->tmem_base;
 
-    // The query rows are in flight since the set-up; warp 0 starts streaming
-    // keys at once.  Decode: each rank of the cluster quantises 64 / cluster
-    // of the 64 head rows (warp 2) and warps 1..7 send them, as one contiguous
-    // run of the 128-byte swizzled B tile (row r is bytes [128 r, 128 r + 128))
-    // plus the rows' weights, to every rank as st.async counted on that
-    // rank's qready.  Prefill: warps 1..19 build the whole tile and meet on a
-    // named barrier.
+    // The query rows are in flight since the set-up; warps 0 and 3 (decode)
+    // start streaming keys at once.  Decode: each rank of the cluster
+    // quantises 64 / cluster of the 64 head rows (warps 4..7) and warps 1, 2
+    // and 4..7 send them, as one contiguous run of the 128-byte swizzled B
+    // tile (row r is bytes [128 r, 128 r + 128)) plus the rows' weights, to
+    // every rank as st.async counted on that rank's qready.  Prefill: warps
+    // 1..19 build the whole tile and meet on a named barrier.
     int qrow0 = 0, qrows = 0;
     if constexpr (kDecode) {
         qrows = 64 / p.cluster;
         qrow0 = static_cast<int>(cluster_rank()) * qrows;
-        // 16 threads per row (warps 2 and up) quantise this rank's rows
-        const int i = tid - 64;
-        if (i >= 0 && i < qrows * 16) {
+        // 16 threads per row (warps 4..7) quantise this rank's rows
+        for (int i = tid - 128; i >= 0 && i < qrows * 16; i += kThreads - 128) {
             const int r = qrow0 + (i >> 4), part = i & 15;
             const unsigned gmask = 0xFFFFu << (threadIdx.x & 16);
             if (!mbar_wait(qbar, 0, status, &ks->abort)) ks->abort = 1;
@@ -510,15 +511,17 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
                                                        qtile, r, 64);
             if (part == 0) wq[r] = wn;
         }
-        // warps 1.. meet on a named barrier and then on the cluster barrier;
-        // warp 0 goes straight to the key loads (they touch only this CTA's
-        // shared memory) and waits on the cluster barrier after its loop
-        if (warp != 0) {
-            asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");
+        // warps 1, 2 and 4..7 meet on a named barrier and then on the cluster
+        // barrier; warps 0 and 3 go straight to the key loads (they touch only
+        // this CTA's shared memory) and wait on the cluster barrier after
+        // their loops
+        if (warp != 0 && warp != 3) {
+            asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 64) : "memory");
             cluster_wait();
             const int run = qrows * 128 / 16;                  // 16-byte chunks per half
             const int per_rank = run * (kFp8 ? 1 : 2) + qrows * 4 / 16;
-            for (int j = tid - 32; j < per_rank * p.cluster; j += kThreads - 32) {
+            const int sender = warp < 3 ? tid - 32 : tid - 64;  // 0 .. kThreads - 65
+            for (int j = sender; j < per_rank * p.cluster; j += kThreads - 64) {
                 const int rk = j / per_rank, c = j - rk * per_rank;
                 const uint32_t qb = dsmem_addr(qready, static_cast<uint32_t>(rk));
                 const uint8_t* src;
@@ -540,41 +543,45 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
 
     // ------------------------------------------------------------ main loop
     if (warp == 0) {
-        // Warp 0: lane 0 issues the key TMA; the whole warp prefetches the
-        // block ids of up to kBidWindow blocks at a time into shared memory,
-        // so no tile waits on a block-table load.
+        // Warp 0: the whole warp loads the block ids of up to kBidWindow
+        // blocks at a time into shared memory, then lane 0 alone issues the
+        // key TMA of every tile whose blocks lie in that window (the chunk
+        // starts on a tile boundary and the window holds whole tiles), with
+        // the stage and phase kept as running counters.  The issue loop is a
+        // single thread's dependent chain and was the decode loop's limit, so
+        // in decode (one window holds a whole chunk) it is split: lane 0 of
+        // warp 0 takes the first half of every tile's blocks and counts the
+        // tile's bytes, lane 0 of warp 3 the second half (see below).
         int* bids = reinterpret_cast<int*>(smem + plan.bid_off);
         const uint64_t pol = kDecode ? policy_evict_first() : policy_evict_last();
+        const int lb_begin = key_begin / kBs;
         const int lb_end = (key_end + kBs - 1) / kBs;
-        int lb_lo = 0, lb_hi = 0;          // window of prefetched logical blocks
-        int t = 0;
-        for (; t < ntiles; ++t) {
-            const int s = t % kStages;
-            const uint32_t ph = static_cast<uint32_t>(t / kStages) & 1u;
-            const int key0 = key_begin + t * kTileKeys;
-            const int lb0 = key0 / kBs;
-            if (lb0 + kBlocksPerTile > lb_hi && lb_hi < lb_end) {
-                __syncwarp();
-                lb_lo = lb0;
-                lb_hi = min(lb_end, lb0 + kBidWindow);
-                for (int i = lane; i < lb_hi - lb_lo; i += 32) {
-                    const int lb = lb_lo + i;
-                    bids[i] = (lb < p.mbps) ? p.block_table[static_cast<int64_t>(seq_b) * p.mbps + lb] : -1;
-                }
-                __syncwarp();
+        const int* bt_row = p.block_table + static_cast<int64_t>(seq_b) * p.mbps;
+        int t = 0;   // tiles issued
+        bool ok = true;
+        for (int w0 = lb_begin; ok && w0 < lb_end; w0 += kBidWindow) {
+            const int wn = min(kBidWindow, lb_end - w0);
+            __syncwarp();
+            for (int i = lane; i < wn; i += 32) bids[i] = (w0 + i < p.mbps) ? bt_row[w0 + i] : -1;
+            __syncwarp();
+            if constexpr (kDecode) {
+                if (lane == 0) mbar_arrive(bready);
             }
-            bool ok = true;
             if (lane == 0) {
-                if (t >= kStages) ok = mbar_wait(&empty[s], ph ^ 1u, status, &ks->abort);
-                if (ok) {
+                int s = t % kStages;
+                uint32_t ph = static_cast<uint32_t>(t / kStages) & 1u;
+                for (int b0 = 0; b0 < wn; b0 += kBlocksPerTile) {
+                    if (t >= kStages && !mbar_wait(&empty[s], ph ^ 1u, status, &ks->abort)) {
+                        ok = false;
+                        break;
+                    }
                     int phys[kBlocksPerTile];
                     uint32_t bytes = 0;
 #pragma unroll
                     for (int j = 0; j < kBlocksPerTile; ++j) {
-                        const int lb = lb0 + j;
                         phys[j] = -1;
-                        if (lb * kBs < key_end) {
-                            const int pb = bids[lb - lb_lo];
+                        if (b0 + j < wn) {
+                            const int pb = bids[b0 + j];
                             if (pb < 0 || pb >= p.num_blocks) {
                                 ks->bad = 1;
                                 set_status(status, IDX_ERR_DEVICE_CHECK);
@@ -587,7 +594,7 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
                     uint8_t* a_s = a_tiles + s * plan.a_stage_bytes;
                     mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
-                    for (int j = 0; j < kBlocksPerTile; ++j) {
+                    for (int j = 0; j < (kDecode ? kBlocksPerTile / 2 : kBlocksPerTile); ++j) {
                         if (phys[j] < 0) continue;
                         if constexpr (kFp8) {
                             tma_load_3d(a_s + j * kBs * 128, &tmap, &full[s], 0, 0, phys[j], pol);
@@ -599,9 +606,15 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
                             tma_load_3d(a_s + 16384 + j * kBs * 128, &tmap, &full[s], 64, 0, phys[j], pol);
                         }
                     }
+                    ++t;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            t = __shfl_sync(0xffffffffu, t, 0);
         }
         if (lane == 0) {
             // copies still in flight (only when a wait gave up) must land before exit
@@ -651,6 +664,51 @@ __global__ void __launch_bounds__(BlockDim<kQT>::value, 1) __maxnreg__(RegCap<kQ
         // every MMA issued above has finished once mdone completes
         mma_commit(mdone);
         mbar_wait(mdone, 0, status, nullptr);
+    } else if (kDecode && warp == 3) {
+        // Decode: the second key issuer, for the second half of every tile's
+        // blocks (warp 0 counts the whole tile's bytes, so these copies may
+        // land before its expect-tx: the phase cannot complete before that
+        // arrival).  A decode chunk is at most 8192 keys, at most 256 blocks
+        // of 32 keys: one window of block ids holds it all.
+        static_assert(8192 / 32 <= kBidWindow, "one block-id window per decode chunk");
+        if (lane == 0 && ntiles > 0) {
+            const int* bids = reinterpret_cast<const int*>(smem + plan.bid_off);
+            const uint64_t pol = policy_evict_first();
+            const int nblk = (key_end + kBs - 1) / kBs - key_begin / kBs;
+            int t = 0;   // tiles issued
+            if (mbar_wait(bready, 0, status, &ks->abort)) {
+                int s = 0;
+                uint32_t ph = 0;
+                for (int b0 = 0; b0 < nblk; b0 += kBlocksPerTile) {
+                    if (t >= kStages && !mbar_wait(&empty[s], ph ^ 1u, status, &ks->abort)) break;
+                    uint8_t* a_s = a_tiles + s * plan.a_stage_bytes;
+#pragma unroll
+                    for (int j = kBlocksPerTile / 2; j < kBlocksPerTile; ++j) {
+                        const int pb = b0 + j < nblk ? bids[b0 + j] : -1;
+                        if (pb < 0 || pb >= p.num_blocks) continue;   // warp 0 flags a bad id
+                        if constexpr (kFp8) {
+                            tma_load_3d(a_s + j * kBs * 128, &tmap, &full[s], 0, 0, pb, pol);
+                            bulk_load(scales + s * 128 + j * kBs,
+                                      p.pool + static_cast<int64_t>(pb) * p.block_bytes + kBs * 128, kBs * 4,
+                                      &full[s], pol);
+                        } else {
+                            tma_load_3d(a_s + j * kBs * 128, &tmap, &full[s], 0, 0, pb, pol);
+                            tma_load_3d(a_s + 16384 + j * kBs * 128, &tmap, &full[s], 64, 0, pb, pol);
+                        }
+                    }
+                    ++t;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // copies still in flight (only when a wait gave up) must land before exit
+            for (int u = max(0, t - kStages); u < t; ++u)
+                mbar_wait(&full[u % kStages], static_cast<uint32_t>(u / kStages) & 1u, status, nullptr);
+        }
+        __syncwarp();
+        cluster_wait();
     } else if (warp >= 4) {
         // epilogue: one key row per thread; warp w reads TMEM lane quadrant
         // w % 4 and queries j0 .. j0 + kQPer - 1 of the tile
