@@ -44,9 +44,9 @@ N_POOL_COPIES = 9
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources they were taken on; a stale hash reports null.
 NCU_TRAFFIC = {
-    ("decode", "02c9d96ab9142728"): 31450624 + 0,
-    ("longctx", "02c9d96ab9142728"): 277265664 + 3192320,
-    ("prefill", "02c9d96ab9142728"): 139508224 + 528729856,   # the scoring kernel
+    ("decode", "daf91faa3c70f719"): 31459072 + 0,
+    ("longctx", "daf91faa3c70f719"): 277265664 + 2918912,
+    ("prefill", "daf91faa3c70f719"): 140015104 + 528819456,   # the scoring kernel
 }
 
 
