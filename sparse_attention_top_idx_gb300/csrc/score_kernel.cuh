@@ -23,8 +23,10 @@
 // fp8 keys use kind::f8f6f4 (e4m3 x e4m3), bf16 keys kind::f16.
 //
 // Warp roles: warp 0 lane 0 starts the query rows' bulk copy, then issues the
-// key TMA (the warp prefetches block ids); the other warps quantise the
-// queries into the B tile; warp 1 owns TMEM and its lane 0 issues the MMAs;
+// key TMA (the warp prefetches block ids; in decode lane 0 of warp 3 issues
+// the second half of every tile's blocks); the other warps quantise the
+// queries into the B tile (decode: warps 4..7, then warps 1, 2 and 4..7 send
+// them to the cluster); warp 1 owns TMEM and its lane 0 issues the MMAs;
 // warps 4.. (decode 4, prefill 16: one per TMEM lane quadrant and query, one
 // key row per thread) run the epilogue ks[s] * sum_h w'[t, h] * max(D, 0)
 // with the query's head weights held in registers.
