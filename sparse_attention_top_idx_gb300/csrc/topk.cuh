@@ -100,22 +100,6 @@ struct SelectSmem {
     uint64_t thr;        // composite threshold of the boundary refinement
 };
 
-// Append c to buf (shared counter *cnt, capacity cap) for the lanes with
-// `take`; one shared atomic per warp.  Every lane of the warp must call it.
-// The counter still advances past cap, so callers can detect overflow.
-__device__ __forceinline__ void warp_append(uint64_t* buf, uint32_t* cnt, uint32_t cap, uint64_t c,
-                                            bool take) {
-    const unsigned m = __ballot_sync(0xffffffffu, take);
-    if (m == 0u) return;
-    const int lane = threadIdx.x & 31;
-    const int leader = __ffs(m) - 1;
-    uint32_t base = 0;
-    if (lane == leader) base = atomicAdd(cnt, static_cast<uint32_t>(__popc(m)));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    const uint32_t pos = base + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
-    if (take && pos < cap) buf[pos] = c;
-}
-
 // Block-wide stream compaction without atomics: every composite c of the walk
 // with valid && take(c) goes to dst (the first `cap` of them), thread t's in
 // walk order after those of threads < t.  Two passes over the walk (count,
@@ -269,26 +253,6 @@ __device__ __forceinline__ void walk_smem(const uint64_t* a, uint32_t n, F f) {
     }
 }
 
-// A global array of n composites, eight independent loads in flight per thread.
-template <class F>
-__device__ __forceinline__ void walk_global(const uint64_t* a, uint32_t n, F f) {
-    constexpr uint32_t U = 8;
-    const unsigned long long* p = reinterpret_cast<const unsigned long long*>(a);
-    for (uint32_t b0 = 0; b0 < n; b0 += kTopkThreads * U) {
-        unsigned long long v[U];
-#pragma unroll
-        for (uint32_t u = 0; u < U; ++u) {
-            const uint32_t i = b0 + u * kTopkThreads + threadIdx.x;
-            v[u] = (i < n) ? __ldcg(p + i) : 0ull;
-        }
-#pragma unroll
-        for (uint32_t u = 0; u < U; ++u) {
-            const uint32_t i = b0 + u * kTopkThreads + threadIdx.x;
-            f(static_cast<uint64_t>(v[u]), i < n);
-        }
-    }
-}
-
 // A global row of n fp32 scores (16-byte aligned, readable up to n rounded up
 // to 4): candidate i is (score_key(row[i]), i).  Four float4 loads in flight
 // (measured best: eight or sixteen made the select slower, two no faster).
@@ -314,16 +278,8 @@ __device__ __forceinline__ void walk_row(const float* row, int n, F f) {
     }
 }
 
-// Compact walks over the same candidates, one load per iteration: for the
-// rare paths that walk the candidates again (small code, slow).
-template <class F>
-__device__ __forceinline__ void walk_global_slow(const uint64_t* a, uint32_t n, F f) {
-#pragma unroll 1
-    for (uint32_t b0 = 0; b0 < n; b0 += kTopkThreads) {
-        const uint32_t i = b0 + threadIdx.x;
-        f(i < n ? static_cast<uint64_t>(__ldcg(reinterpret_cast<const unsigned long long*>(a) + i)) : 0ull, i < n);
-    }
-}
+// A compact walk over the same row, one load per iteration: for the rare
+// paths that walk the candidates again (small code, slow).
 template <class F>
 __device__ __forceinline__ void walk_row_slow(const float* row, int n, F f) {
 #pragma unroll 1
@@ -363,111 +319,6 @@ __device__ uint64_t radix_refine(Each each, int bin, uint32_t m, SelectSmem* ss)
         if (at == need) break;  // every member with this prefix is selected
     }
     return prefix;
-}
-
-// In-place bitonic sort, descending, of n (power of two, <= 4096) composites.
-__device__ __forceinline__ void bitonic_sort_desc(uint64_t* a, int n) {
-    for (int size = 2; size <= n; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < n / 2; i += kTopkThreads) {
-                int lo = 2 * i - (i & (stride - 1));
-                int hi = lo + stride;
-                bool desc = ((lo & size) == 0);
-                uint64_t x = a[lo], y = a[hi];
-                if ((x < y) == desc) {
-                    a[lo] = y;
-                    a[hi] = x;
-                }
-            }
-            __syncthreads();
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Block sort, descending, of 256 * E composites held E per thread (thread t
-// owns positions t*E .. t*E+E-1).  Bitonic network: compare-exchanges between
-// a thread's own registers, then across lanes with warp shuffles, and through
-// shared memory (two block barriers a stage) only for strides that cross
-// warps: for 4096 keys, 6 of the 78 stages.  In shared memory position
-// t*E + e lives at word e*256 + t, so that the 32 lanes of a warp touch 32
-// consecutive words (no bank conflicts) in every exchange.
-// ---------------------------------------------------------------------------
-template <int E, int SIZE, int STRIDE>
-__device__ __forceinline__ void bsort_stage(uint64_t (&v)[E], uint64_t* a) {
-    const int t = threadIdx.x;
-    if constexpr (STRIDE >= 32 * E) {
-        // partner of position t*E + e is (t ^ STRIDE/E)*E + e: same e, other thread
-#pragma unroll
-        for (int e = 0; e < E; ++e) a[e * kTopkThreads + t] = v[e];
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int i = t * E + e;
-            const uint64_t p = a[e * kTopkThreads + (t ^ (STRIDE / E))];
-            const bool keep_max = ((i & STRIDE) == 0) == ((i & SIZE) == 0);
-            v[e] = keep_max ? (v[e] > p ? v[e] : p) : (v[e] < p ? v[e] : p);
-        }
-        __syncthreads();
-    } else if constexpr (STRIDE >= E) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int i = t * E + e;
-            const uint64_t p = __shfl_xor_sync(0xffffffffu, static_cast<unsigned long long>(v[e]), STRIDE / E);
-            const bool keep_max = ((i & STRIDE) == 0) == ((i & SIZE) == 0);
-            v[e] = keep_max ? (v[e] > p ? v[e] : p) : (v[e] < p ? v[e] : p);
-        }
-    } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            if ((e & STRIDE) == 0) {
-                const bool desc = ((t * E + e) & SIZE) == 0;
-                const uint64_t x = v[e], y = v[e + STRIDE];
-                if ((x < y) == desc) {
-                    v[e] = y;
-                    v[e + STRIDE] = x;
-                }
-            }
-        }
-    }
-}
-template <int E, int SIZE, int STRIDE>
-__device__ __forceinline__ void bsort_strides(uint64_t (&v)[E], uint64_t* a) {
-    bsort_stage<E, SIZE, STRIDE>(v, a);
-    if constexpr (STRIDE > 1) bsort_strides<E, SIZE, STRIDE / 2>(v, a);
-}
-template <int E, int SIZE>
-__device__ __forceinline__ void bsort_sizes(uint64_t (&v)[E], uint64_t* a) {
-    bsort_strides<E, SIZE, SIZE / 2>(v, a);
-    if constexpr (SIZE < kTopkThreads * E) bsort_sizes<E, SIZE * 2>(v, a);
-}
-// Sorts a[0 .. 256*E) in place (shared memory), descending.  All 256 threads.
-// The input order is immaterial, so each thread loads the conflict-free words
-// e*256 + t; only the final store writes position order.
-template <int E>
-__device__ __forceinline__ void block_sort_desc(uint64_t* a) {
-    uint64_t v[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) v[e] = a[e * kTopkThreads + threadIdx.x];
-    bsort_sizes<E, 2>(v, a);
-    __syncthreads();
-#pragma unroll
-    for (int e = 0; e < E; ++e) a[threadIdx.x * E + e] = v[e];
-    __syncthreads();
-}
-// Sorts a[0 .. n) descending for n <= 256 * kMaxE; entries up to the next
-// size step (256, 512, ...) are overwritten with zero padding.
-template <int kMaxE>
-__device__ __forceinline__ void block_sort_desc_n(uint64_t* a, int n) {
-    int n2 = kTopkThreads;
-    while (n2 < n) n2 <<= 1;
-    for (int i = n + static_cast<int>(threadIdx.x); i < n2; i += kTopkThreads) a[i] = 0ull;
-    __syncthreads();
-    if (n2 <= 256) block_sort_desc<1>(a);
-    else if (n2 <= 512) block_sort_desc<2>(a);
-    else if (n2 <= 1024) block_sort_desc<4>(a);
-    else if (kMaxE <= 8 || n2 <= 2048) block_sort_desc<(kMaxE < 8 ? kMaxE : 8)>(a);
-    else block_sort_desc<kMaxE>(a);
 }
 
 // ---------------------------------------------------------------------------
