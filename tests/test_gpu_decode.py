@@ -163,6 +163,25 @@ def test_bad_block_id_flags_row():
     check_rows(got, ref, nvis, 64, rows=[0])
 
 
+@pytest.mark.parametrize("bs", [32, 64])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_bad_block_ids_on_either_key_issuer(bs, mode):
+    # Two lanes issue a decode tile's key copies: one the first half of its
+    # blocks (and the tile's byte count), the other the second half.  A bad
+    # id in either half flags only its own sequence.  2000 keys over 8 CTAs
+    # give 256-key chunks, two tiles each; the ids hit rank 0's second tile.
+    W = wl.make_workload("bad2", [2000, 2000, 1000], [1, 1, 1], topk=64, bs=bs, seed=12 + bs + mode)
+    cache = build_cache(W, mode)
+    per_tile = 128 // bs
+    W.block_table[0, per_tile + per_tile // 2 - 1] = W.num_blocks + 3   # last of the first half
+    W.block_table[1, per_tile + per_tile // 2] = -2                     # first of the second half
+    got = run_decode(W, mode, cache=cache, expect_status=5)
+    assert np.all(got["idx"][0] == -1)
+    assert np.all(got["idx"][1] == -1)
+    ref, nvis = oracle_ref(W, mode, [2])
+    check_rows(got, ref, nvis, 64, rows=[2])
+
+
 def test_seq_len_above_bound_flags_row():
     W = wl.make_workload("over", [1000, 600], [1, 1], topk=64, seed=10)
     got = run_decode(W, dsaidx.FP8, max_seq_len=800, expect_status=5)
