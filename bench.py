@@ -310,34 +310,49 @@ def load_padding(graph, seconds, device):
         torch.cuda.synchronize(device)
 
 
+def pack_pinned(tensors, device, align=256, pin=True):
+    """One pinned host buffer and one device buffer holding `tensors` back to
+    back (each at an `align`-byte offset), and device views of every part, so a
+    step's inputs cross to the device in a single copy.  Returns (host, dev,
+    views)."""
+    import torch
+    offs, o = [], 0
+    for t in tensors:
+        o = (o + align - 1) // align * align
+        offs.append(o)
+        o += t.numel() * t.element_size()
+    host = torch.empty(o, dtype=torch.uint8)
+    if pin:
+        host = host.pin_memory()
+    dev = torch.empty(o, dtype=torch.uint8, device=device)
+    views = []
+    for t, off in zip(tensors, offs):
+        n = t.numel() * t.element_size()
+        host[off:off + n].copy_(t.detach().cpu().contiguous().reshape(-1).view(torch.uint8))
+        views.append(dev[off:off + n].view(t.dtype).view(t.shape))
+    return host, dev, views
+
+
 def e2e_decode(bench, steps, warmup, device):
-    """Same decode step through the public API from pinned host buffers: every
+    """Same decode step through the public API from pinned host memory: every
     step copies the step's inputs host->device (queries, head weights, sequence
-    lengths, the new keys and their slots), stores the keys, scores and selects,
-    and copies the selected indices back to the host.  Timed twice: replayed
-    from a CUDA graph (how a serving decode loop issues it) and issued eagerly
-    from Python call by call."""
+    lengths, the new keys and their slots, packed in one pinned buffer and sent
+    as one copy), stores the keys, scores and selects, and copies the selected
+    indices back to the host.  Timed twice: replayed from a CUDA graph (how a
+    serving decode loop issues it) and issued eagerly from Python call by
+    call."""
     import torch
     W = bench.W
-    h_q = bench.q.cpu().pin_memory()
-    h_w = bench.w.cpu().pin_memory()
-    h_sl = bench.sl.cpu().pin_memory()
-    h_k = bench.new_k.cpu().pin_memory()
-    h_s = bench.new_slots.cpu().pin_memory()
+    h_in, d_in, (d_q, d_w, d_sl, d_k, d_s) = pack_pinned(
+        [bench.q, bench.w, bench.sl, bench.new_k, bench.new_slots], device)
     h_out = torch.empty_like(bench.out, device="cpu").pin_memory()
-    d_q, d_w, d_sl = torch.empty_like(bench.q), torch.empty_like(bench.w), torch.empty_like(bench.sl)
-    d_k, d_s = torch.empty_like(bench.new_k), torch.empty_like(bench.new_slots)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_w, h_sl, h_k, h_s))
+    h2d = h_in.numel()
     d2h = h_out.numel() * h_out.element_size()
     ds = bench.dsaidx
 
     def one(i, ev=None):
         c = bench.caches[i % len(bench.caches)]
-        d_q.copy_(h_q, non_blocking=True)
-        d_w.copy_(h_w, non_blocking=True)
-        d_sl.copy_(h_sl, non_blocking=True)
-        d_k.copy_(h_k, non_blocking=True)
-        d_s.copy_(h_s, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         ds.store_keys(c, d_k, d_s)
         ds.score_topk_decode(c, d_q, d_w, bench.bt, d_sl, bench.msl, W.topk, bench.out, bench.ws)
         h_out.copy_(bench.out, non_blocking=True)

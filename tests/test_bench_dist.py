@@ -53,3 +53,19 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
 
 def test_whole_job_rate_single_rank():
     assert bench.whole_job_rate(1, 232000, 0.5) == pytest.approx(232000 / 0.5e-3)
+
+
+def test_packed_inputs_round_trip():
+    # the end-to-end step sends its inputs as one buffer: every part's view
+    # must hold that input, at an aligned offset, after the single copy
+    import torch
+    parts = [torch.randn(3, 64, 128).to(torch.bfloat16), torch.randn(3, 64), torch.tensor([5, 7, 9], dtype=torch.int32),
+             torch.randn(3, 128).to(torch.bfloat16), torch.tensor([11, 12, 13], dtype=torch.int64)]
+    host, dev, views = bench.pack_pinned(parts, "cpu", pin=False)
+    dev.zero_()
+    dev.copy_(host)
+    for t, v in zip(parts, views):
+        assert v.dtype == t.dtype and v.shape == t.shape
+        assert torch.equal(v, t)
+        assert (v.data_ptr() - dev.data_ptr()) % 256 == 0
+    assert host.numel() == dev.numel() >= sum(t.numel() * t.element_size() for t in parts)
