@@ -177,11 +177,13 @@ idx_status idx_score_topk_decode(const idx_cache* cache, const void* q_bf16_dev,
  * convenience of this library.)
  *
  * Same arguments, results and errors as idx_score_topk_decode, without
- * workspace_dev / ws_bytes.  The scratch lives in a fixed 8 MiB area of
+ * workspace_dev / ws_bytes.  The scratch lives in a fixed 32 MiB area of
  * library-owned device memory that every GPU loading the library holds until
  * the process exits; a shape whose idx_workspace_bytes_decode() exceeds
- * 8 MiB (roughly batch * (16 KiB + 8 bytes * max_seq_len)) is rejected with
- * IDX_ERR_WORKSPACE_TOO_SMALL before anything runs.  The call allocates
+ * 32 MiB is rejected with IDX_ERR_WORKSPACE_TOO_SMALL before anything runs.
+ * (About 4 bytes per key of the longest sequence per cluster launched, at
+ * most 10 MiB, plus, when sequences span several 65,536-key segments,
+ * batch * (32 KiB + 8 * topk * ceil(max_seq_len / 65536)) bytes.)  The call allocates
  * nothing; it clears the part of the area it uses (an asynchronous memset on
  * `stream`) and launches the decode kernel.
  *  - The first call on each device looks up the area's device address (with
@@ -228,8 +230,21 @@ idx_status idx_score_topk_prefill(const idx_cache* cache, const void* q_bf16_dev
  */
 idx_status idx_read_device_status(const void* workspace_dev, void* stream, int32_t* code_out);
 
-/* Static description of a status code. */
+/* Static description of a status code.  (Library utility; no passage.) */
 const char* idx_status_str(idx_status status);
+
+/*
+ * Test hook for the failure path (library utility; no passage).  Shortens the
+ * limit of the decode kernel's pipeline waits to limit_ns nanoseconds and
+ * makes its MMA issuer withhold the completion signal of the first
+ * accumulator of every CTA, so that a bounded wait runs out: the call then
+ * records IDX_ERR_TIMEOUT in the workspace status, writes -1 rows for the
+ * affected sequences, drains its own copies and MMAs, frees TMEM and returns
+ * (no GPU fault, trap or hang).  0 (or any value >= 2 s) restores the normal
+ * 2 s limit and the normal signalling.  Process-wide; affects calls issued
+ * after it returns.
+ */
+idx_status idx_test_set_wait_limit(unsigned long long limit_ns);
 
 #ifdef __cplusplus
 }

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -44,23 +45,32 @@ bool same_device(const idx_cache* c) {
     return cudaGetDevice(&dev) == cudaSuccess && dev == c->device;
 }
 
-// Decode workspace layout.
+// Decode workspace layout: the status header, the unit counters, per
+// sequence a ticket and a flag, the clusters' slow-path score scratch and,
+// when a sequence can take several segments, per sequence an 8192-bin
+// histogram and nseg_max runs of topk composites.
 struct DecodeWs {
-    size_t ctr, ghist, seqflag, seqcnt, cand, total;
-    int64_t cand_cap;
+    size_t ctr, seqflag, ucount, scratch, ghist, runs, total;
+    int64_t runs_cap;   // composites per sequence
     dsaidx::DecodeGeom geom;
 };
-DecodeWs decode_ws(const idx_cache* c, int batch, int max_seq_len) {
+DecodeWs decode_ws(const idx_cache* c, int batch, int max_seq_len, int topk) {
     DecodeWs w{};
     w.geom = dsaidx::decode_geometry(c, batch, max_seq_len);
     const size_t nb = static_cast<size_t>(batch);
-    w.cand_cap = static_cast<int64_t>(w.geom.nseg_max) * w.geom.cluster * w.geom.chunk;
+    const bool multi = w.geom.nseg_max > 1;
+    w.runs_cap = multi ? static_cast<int64_t>(w.geom.nseg_max) * topk : 0;
+    // clusters launched: at most one per unit and at most kDecMaxClusters
+    const int64_t units = static_cast<int64_t>(batch) * w.geom.nseg_max;
+    const int64_t maxcl = dsaidx::kDecMaxClusters(c->num_sms);
+    const size_t clusters = static_cast<size_t>(units < maxcl ? units : maxcl);
     size_t o = dsaidx::kWsHeaderBytes;
     w.ctr = o;      o = align_up(o + nb * 4, 256);
-    w.ghist = o;    o = align_up(o + nb * dsaidx::kHistBins * 4, 256);
     w.seqflag = o;  o = align_up(o + nb * 4, 256);
-    w.seqcnt = o;   o = align_up(o + nb * 4, 256);
-    w.cand = o;     o = align_up(o + nb * static_cast<size_t>(w.cand_cap) * 8, 256);
+    w.ucount = o;   o = align_up(o + 8, 256);
+    w.scratch = o;  o = align_up(o + clusters * dsaidx::kDecCl * static_cast<size_t>(w.geom.chunk) * 4, 256);
+    w.ghist = o;    o = align_up(o + (multi ? nb * 8192 * 4 : 0), 256);
+    w.runs = o;     o = align_up(o + nb * static_cast<size_t>(w.runs_cap) * 8, 256);
     w.total = o;
     return w;
 }
@@ -81,6 +91,11 @@ PrefillWs prefill_ws(int total_q, int max_seq_len) {
 }
 
 bool valid_dtype(int d) { return d == IDX_KEY_FP8_E4M3 || d == IDX_KEY_BF16; }
+
+// Limit of the decode kernel's pipeline waits; idx_test_set_wait_limit
+// shortens it (and makes the MMA issuer withhold one signal) for the test of
+// the timeout path.
+std::atomic<unsigned long long> g_test_wait_ns{dsaidx::kWaitLimitNs};
 
 }  // namespace
 
@@ -152,7 +167,7 @@ idx_status idx_store_keys(const idx_cache* cache, const void* k_bf16_dev, const 
 size_t idx_workspace_bytes_decode(const idx_cache* cache, int batch, int max_seq_len, int heads, int topk) {
     if (!cache || batch < 0 || max_seq_len < 0 || heads != dsaidx::kHeads) return 0;
     if (topk < 1 || topk > IDX_MAX_TOPK) return 0;
-    return decode_ws(cache, batch, max_seq_len).total;
+    return decode_ws(cache, batch, max_seq_len, topk).total;
 }
 
 idx_status idx_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream) {
@@ -177,10 +192,9 @@ idx_status idx_score_topk_decode(const idx_cache* cache, const void* q_bf16_dev,
     if (!aligned(q_bf16_dev, 16) || !aligned(w_dev, 16) || !aligned(workspace_dev, 256))
         return IDX_ERR_INVALID_ARG;
     if (!same_device(cache)) return IDX_ERR_INVALID_ARG;
-    const DecodeWs ws = decode_ws(cache, batch, max_seq_len);
+    const DecodeWs ws = decode_ws(cache, batch, max_seq_len, topk);
     if (ws_bytes < ws.total) return IDX_ERR_WORKSPACE_TOO_SMALL;
-    if (static_cast<int64_t>(batch) * ws.geom.nseg_max * ws.geom.cluster >= (int64_t(1) << 31))
-        return IDX_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(batch) * ws.geom.nseg_max >= (int64_t(1) << 31)) return IDX_ERR_INVALID_ARG;
     uint8_t* base = static_cast<uint8_t*>(workspace_dev);
     dsaidx::ScoreParams p{};
     p.q = static_cast<const uint16_t*>(q_bf16_dev);
@@ -201,11 +215,14 @@ idx_status idx_score_topk_decode(const idx_cache* cache, const void* q_bf16_dev,
     p.out_score = out_score_dev;
     p.status = reinterpret_cast<int32_t*>(base);
     p.ctr = reinterpret_cast<uint32_t*>(base + ws.ctr);
-    p.ghist = reinterpret_cast<uint32_t*>(base + ws.ghist);
     p.seqflag = reinterpret_cast<uint32_t*>(base + ws.seqflag);
-    p.seqcnt = reinterpret_cast<uint32_t*>(base + ws.seqcnt);
-    p.cand = reinterpret_cast<uint64_t*>(base + ws.cand);
-    p.cand_cap = ws.cand_cap;
+    p.ghist = reinterpret_cast<uint32_t*>(base + ws.ghist);
+    p.cand = reinterpret_cast<uint64_t*>(base + ws.runs);
+    p.cand_cap = ws.runs_cap;
+    p.ucount = reinterpret_cast<uint32_t*>(base + ws.ucount);
+    p.scratch = reinterpret_cast<float*>(base + ws.scratch);
+    p.wait_ns = g_test_wait_ns.load(std::memory_order_relaxed);
+    p.withhold = p.wait_ns != dsaidx::kWaitLimitNs ? 1 : 0;
     cudaError_t e = dsaidx::launch_decode(cache, p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
@@ -261,6 +278,7 @@ idx_status idx_score_topk_prefill(const idx_cache* cache, const void* q_bf16_dev
     p.rowflag = reinterpret_cast<uint32_t*>(base + ws.rowflag);
     p.scores = reinterpret_cast<float*>(base + ws.scores);
     p.score_stride = ws.stride;
+    p.wait_ns = dsaidx::kWaitLimitNs;
     cudaError_t e = dsaidx::launch_prefill(cache, p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
@@ -272,6 +290,12 @@ idx_status idx_read_device_status(const void* workspace_dev, void* stream, int32
     int32_t v = 0;
     if (cudaMemcpy(&v, workspace_dev, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return IDX_ERR_CUDA;
     *code_out = v;
+    return IDX_OK;
+}
+
+idx_status idx_test_set_wait_limit(unsigned long long limit_ns) {
+    if (limit_ns == 0 || limit_ns > dsaidx::kWaitLimitNs) limit_ns = dsaidx::kWaitLimitNs;
+    g_test_wait_ns.store(limit_ns, std::memory_order_relaxed);
     return IDX_OK;
 }
 

@@ -133,17 +133,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait for the phase with the given parity to complete.  Returns false
-// (and records IDX_ERR_TIMEOUT) when the limit runs out or when another role
-// of the CTA already gave up (*abort set).
+// (and records IDX_ERR_TIMEOUT) when `limit_ns` of %globaltimer runs out or
+// when another role of the CTA already gave up (*abort set).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
+        // the timer is read every 256 tries, or every try under a shortened limit
+        if ((it & 255u) == 0 || limit_ns < kWaitLimitNs) {
             if (abort_flag && *abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 set_status(status, IDX_ERR_TIMEOUT);
                 if (abort_flag) *abort_flag = 1;
                 return false;
@@ -165,12 +167,13 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int32_t* status) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int32_t* status,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     unsigned long long t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+        if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) {
             set_status(status, IDX_ERR_TIMEOUT);
             return false;
         }

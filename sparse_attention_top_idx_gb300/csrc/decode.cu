@@ -1,32 +1,83 @@
-// decode.cu -- launch of the fused decode score + top-k kernel as thread-block
-// clusters (one cluster per segment of a sequence).
-#include "score_kernel.cuh"
+// decode.cu -- launch of the fused decode score + top-k kernel: a grid of
+// persistent 8-CTA thread-block clusters that take the batch's sequence
+// segments in turn (decode_kernel.cuh).
+#include <mutex>
+
+#include "decode_kernel.cuh"
 
 namespace dsaidx {
 
 namespace {
 
-constexpr int kDecodeCluster = kCl;   // portable cluster size
+constexpr int kMaxDevices = 64;
+
+// A kernel of the decode kernel's shape (threads, registers, dynamic shared
+// memory) that allocates no TMEM: the occupancy calculator counts one CTA per
+// SM for a kernel that allocates TMEM, while two CTAs of 128 TMEM columns
+// each do share an SM (measured on GB300), so clusters are counted on this
+// stand-in.
+__global__ void __maxnreg__(120) decode_shape_probe(int* sink) {
+    if (sink) sink[threadIdx.x] = 0;
+}
+
+struct ClusterFit {
+    std::mutex mu;
+    int n[kMaxDevices] = {};
+};
+
+// Clusters of the decode shape that fit on the device at once (queried once
+// per device and key format, like the shared-memory limit, so that later
+// calls -- including calls captured into a graph -- make no runtime query).
+cudaError_t resident_clusters(int smem, int dev, ClusterFit& fit, int* out) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(fit.mu);
+    int* cached = fit.n;
+    if (cached[dev] == 0) {
+        cudaError_t e = cudaFuncSetAttribute(decode_shape_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kDecCl, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kDecCl;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, decode_shape_probe, &cfg);
+        if (e != cudaSuccess) return e;
+        cached[dev] = n > 0 ? n : 1;
+    }
+    *out = cached[dev];
+    return cudaSuccess;
+}
 
 template <bool kFp8, int kBs>
-cudaError_t launch_decode_t(const idx_cache* c, const ScoreParams& p, cudaStream_t st) {
+cudaError_t launch_decode_t(const idx_cache* c, const ScoreParams& p, int64_t units_bound, cudaStream_t st) {
     static std::atomic<unsigned long long> attr_done{0};
-    const SmemPlan plan = make_plan(kFp8, 1, p.chunk);
-    auto kern = score_kernel<kFp8, kBs, 1>;
-    // the limit is raised once to the largest plan this key format uses
-    int most = make_plan(kFp8, 1, kFp8 ? 8192 : 2048).total;
-    const int mid = make_plan(kFp8, 1, 4096).total;
-    if (kFp8 && mid > most) most = mid;
-    cudaError_t e = set_smem_once(kern, most, attr_done);
+    static ClusterFit clusters;
+    const DecPlan plan = dec_plan(kFp8);
+    auto kern = decode_kernel<kFp8, kBs>;
+    cudaError_t e = set_smem_once(kern, plan.total, attr_done);
     if (e != cudaSuccess) return e;
+    int fit = 1;
+    e = resident_clusters(plan.total, c->device, clusters, &fit);
+    if (e != cudaSuccess) return e;
+    // persistent clusters: at most those that fit at once (and never more
+    // than the workspace's slow-path scratch provides for)
+    int64_t g = units_bound < fit ? units_bound : fit;
+    if (g > kDecMaxClusters(c->num_sms)) g = kDecMaxClusters(c->num_sms);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.batch) * p.nseg_max * p.cluster, 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(g) * kDecCl, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(plan.total);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+    attr[0].val.clusterDim.x = kDecCl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -36,31 +87,26 @@ cudaError_t launch_decode_t(const idx_cache* c, const ScoreParams& p, cudaStream
 
 }  // namespace
 
-// One cluster of 8 CTAs per sequence segment.  A CTA scores at most `chunk`
-// keys: the longest sequence's share of its cluster rounded up to the 128-key
-// tile, at most 8192 (fp8) or 2048 (bf16) keys so that the chunk's scores stay
-// in shared memory; sequences longer than 8 chunks take several segments.
+// Segments of the longest sequence; every sequence takes at most that many
+// units (an empty or invalid one takes one).
 DecodeGeom decode_geometry(const idx_cache* c, int batch, int max_seq_len) {
+    (void)c;
     (void)batch;
     DecodeGeom g{};
-    g.cluster = kDecodeCluster;
-    const int cap = (c->key_dtype == IDX_KEY_FP8_E4M3) ? 8192 : 2048;
-    int64_t per = (static_cast<int64_t>(max_seq_len) + g.cluster - 1) / g.cluster;
-    per = (per + kTileKeys - 1) / kTileKeys * kTileKeys;
-    if (per < kTileKeys) per = kTileKeys;
-    g.chunk = static_cast<int>(per < cap ? per : cap);
-    const int64_t seglen = static_cast<int64_t>(g.cluster) * g.chunk;
-    int64_t nseg = (static_cast<int64_t>(max_seq_len) + seglen - 1) / seglen;
-    g.nseg_max = static_cast<int>(nseg < 1 ? 1 : nseg);
+    g.cluster = kDecCl;
+    g.chunk = max_seq_len > 0 ? dec_chunk(max_seq_len) : kTileKeys;
+    g.nseg_max = max_seq_len > 0 ? dec_nseg(max_seq_len) : 1;
     return g;
 }
 
 cudaError_t launch_decode(const idx_cache* c, const ScoreParams& p, cudaStream_t st) {
+    const int64_t units_bound = static_cast<int64_t>(p.batch) * p.nseg_max;
+    if (units_bound <= 0) return cudaSuccess;
     const bool fp8 = c->key_dtype == IDX_KEY_FP8_E4M3;
-    if (fp8 && c->block_size == 64) return launch_decode_t<true, 64>(c, p, st);
-    if (fp8 && c->block_size == 32) return launch_decode_t<true, 32>(c, p, st);
-    if (!fp8 && c->block_size == 64) return launch_decode_t<false, 64>(c, p, st);
-    return launch_decode_t<false, 32>(c, p, st);
+    if (fp8 && c->block_size == 64) return launch_decode_t<true, 64>(c, p, units_bound, st);
+    if (fp8 && c->block_size == 32) return launch_decode_t<true, 32>(c, p, units_bound, st);
+    if (!fp8 && c->block_size == 64) return launch_decode_t<false, 64>(c, p, units_bound, st);
+    return launch_decode_t<false, 32>(c, p, units_bound, st);
 }
 
 }  // namespace dsaidx

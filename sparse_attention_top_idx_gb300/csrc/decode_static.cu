@@ -14,7 +14,7 @@ namespace {
 
 // Largest scratch a call may need; every GPU that loads the library holds this
 // much device memory until the process exits.
-constexpr size_t kStaticScratchBytes = static_cast<size_t>(8) << 20;   // 8 MiB
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(32) << 20;   // 32 MiB
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 

@@ -53,47 +53,103 @@ struct ScoreParams {
     float* out_score;
     // workspace
     int32_t* status;
-    uint32_t* ctr;               // decode: [batch] completed-chunk tickets
-    uint32_t* ghist;             // decode: [batch, 4096] histogram of published candidates
-    uint32_t* seqflag;           // decode: [batch] device-check flags
-    uint32_t* seqcnt;            // decode: [batch] candidates published per sequence
-    uint64_t* cand;              // decode: [batch, cand_cap] composites
-    int64_t cand_cap;            // decode: nseg_max * cluster * chunk (>= every seq_len)
+    uint32_t* ctr;               // decode: [batch] completed-segment tickets
+    uint32_t* ghist;             // decode: [batch, 8192] bin counts of the segments' runs
+    uint32_t* seqflag;           // decode: [batch] a segment failed a device check
+    uint64_t* cand;              // decode: [batch, cand_cap] the segments' sorted top-k runs
+    int64_t cand_cap;            // decode: nseg_max * topk composites per sequence
     float* scores;               // prefill: [total_q, score_stride]
     int64_t score_stride;
     uint32_t* rowflag;           // prefill: [total_q]
+    uint32_t* ucount;            // decode: [2] units drawn, clusters done (zero between calls)
+    float* scratch;              // decode: per cluster kDecCl * chunk scores (slow path)
+    unsigned long long wait_ns;  // limit of the pipeline waits (normally 2 s)
+    int withhold;                // test hook: 1 = the MMA issuer withholds its first accumulator signal
 };
 
-// Shared-memory plan of the scoring kernel for (fp8, queries per CTA, chunk).
+// ---------------------------------------------------------------------------
+// decode geometry (host and device agree on it)
+// ---------------------------------------------------------------------------
+constexpr int kDecCl = 8;               // CTAs per cluster (one sequence segment)
+constexpr int kDecChunkMax = 8192;      // keys one CTA scores per segment
+
+// Keys per CTA for a sequence of S > 0 keys: its share of a cluster rounded up
+// to the 128-key tile, at most kDecChunkMax.
+__host__ __device__ inline int dec_chunk(int S) {
+    int per = (S + kDecCl - 1) / kDecCl;
+    per = (per + kTileKeys - 1) / kTileKeys * kTileKeys;
+    if (per < kTileKeys) per = kTileKeys;
+    return per < kDecChunkMax ? per : kDecChunkMax;
+}
+// Segments (clusters' worth of chunks) of a sequence of S > 0 keys.
+__host__ __device__ inline int dec_nseg(int S) {
+    const int64_t seglen = static_cast<int64_t>(kDecCl) * dec_chunk(S);
+    const int64_t n = (static_cast<int64_t>(S) + seglen - 1) / seglen;
+    return n < 1 ? 1 : static_cast<int>(n);
+}
+// Work units of a sequence: its segments, or one unit that writes the -1 row
+// of an empty sequence or of one whose length is out of range.
+__host__ __device__ inline int dec_units(int S, int max_seq_len) {
+    return (S > 0 && S <= max_seq_len) ? dec_nseg(S) : 1;
+}
+
+// Shared-memory plan of the decode kernel: the key stages (after the stream:
+// the selection's candidate lists and scratch); one region that holds in turn
+// the staged bf16 query rows, the chunk's 16-bit histogram (during the
+// stream) and the pool of every CTA's sorted candidates (during the
+// selection); the chunk's scores; the cluster's histogram windows; the B
+// tile, w', block ids, scratch and barriers.  fp8: about 99 KB, two CTAs per
+// SM; bf16: one.
+struct DecPlan {
+    int stages, a_stage_bytes, a_off, raw_off, sc_off, win_off, pool_off, q_off, w_off, bid_off, misc_off, bar_off,
+        total;
+};
+__host__ __device__ inline DecPlan dec_plan(bool fp8) {
+    DecPlan p{};
+    p.stages = 2;
+    p.a_stage_bytes = fp8 ? 16384 : 32768;
+    int o = 0;
+    p.a_off = o;      o += p.stages * p.a_stage_bytes;
+    p.raw_off = o;    o += 64 * 256 + 64 * 4;          // >= the 16 KB histogram and the 16 KB pool
+    p.pool_off = p.raw_off;
+    p.sc_off = o;     o += kDecChunkMax * 4 + 16;
+    p.win_off = o;    o += kDecCl * 528;
+    o = (o + 1023) / 1024 * 1024;
+    p.q_off = o;      o += 64 * (fp8 ? 128 : 256);
+    p.w_off = o;      o += 64 * 4;
+    p.bid_off = o;    o += kDecChunkMax / 32 * 4;   // block ids of one chunk
+    p.misc_off = o;   o += 4096;
+    p.bar_off = o;    o += 256;
+    p.total = o + 1024;
+    return p;
+}
+static_assert(2 * 16384 >= 4096 * 8, "the selection buffer fits the fp8 key stages");
+static_assert(kDecChunkMax * 4 >= 4096 * 4, "the selection histogram fits the chunk's score area");
+constexpr int kDecMaxClusters(int sms) { return 2 * sms / kDecCl; }   // two CTAs per SM at most
+
+// Shared-memory plan of the prefill scoring kernel (kPrefillQT queries per
+// CTA): key stages, the B tile, key scales, head weights, the staged bf16
+// query rows, block ids, scratch and barriers.
 struct SmemPlan {
     int stages, a_stage_bytes, q_bytes, n_cols;
-    int a_off, recv_off, recv_bytes, q_off, scale_off, w_off, hist_off, raw_off, bid_off, misc_off, bar_off;
+    int a_off, q_off, scale_off, w_off, raw_off, bid_off, misc_off, bar_off;
     int total;   // bytes to request (includes 1 KB of alignment slack)
 };
-
-// Decode keeps two CTAs per SM (<= ~112 KB each for fp8 keys): while the
-// chunk's scores take <= 16 KB, three key stages and a 16 KB area that
-// receives the other CTAs' histogram slices at the end (cluster_select);
-// three stages for larger chunks.  The raw query rows are staged where the
-// decode scores later go (or, for prefill, in a 64 KB region of their own).
 __host__ __device__ inline SmemPlan make_plan(bool fp8, int qt, int chunk) {
+    (void)chunk;
     SmemPlan p{};
     p.n_cols = 64 * qt;
-    p.stages = (qt == 1) ? (fp8 ? 3 : 2) : (fp8 ? 4 : 2);
-    p.recv_bytes = (qt == 1 && fp8 && chunk <= 4096) ? 16384 : 0;
+    p.stages = fp8 ? 4 : 2;
     p.a_stage_bytes = fp8 ? 16384 : 32768;
     p.q_bytes = p.n_cols * (fp8 ? 128 : 256);
-    const int raw_bytes = (qt == 1) ? (chunk * 4 > 16384 ? chunk * 4 : 16384) : qt * 16384;
     int o = 0;
     p.a_off = o;       o += p.stages * p.a_stage_bytes;
-    p.recv_off = o;    o += p.recv_bytes;
     p.q_off = o;       o += p.q_bytes;
     p.scale_off = o;   o += fp8 ? p.stages * 512 : 0;
     p.w_off = o;       o += p.n_cols * 4;
-    p.hist_off = o;    o += (qt == 1) ? 4096 * 4 : 0;
-    p.raw_off = o;     o += raw_bytes;
+    p.raw_off = o;     o += qt * 16384;
     p.bid_off = o;     o += kBidWindow * 4;  // prefetched block ids
-    p.misc_off = o;    o += 4096;            // selection scratch, flags, group scan
+    p.misc_off = o;    o += 4096;            // scratch, flags, group scan
     p.bar_off = o;     o += 512;             // mbarriers
     p.total = o + 1024;
     return p;
@@ -120,8 +176,8 @@ cudaError_t launch_store(const idx_cache* c, const void* k, const int64_t* slots
 cudaError_t launch_decode(const idx_cache* c, const ScoreParams& p, cudaStream_t st);
 cudaError_t launch_prefill(const idx_cache* c, const ScoreParams& p, cudaStream_t st);
 
-// Decode geometry for a batch shape: clusters of `cluster` CTAs, each CTA
-// scoring at most `chunk` keys, `nseg_max` cluster segments per sequence.
+// Decode geometry for a batch shape: clusters of `cluster` CTAs, chunks of at
+// most `chunk` keys, at most `nseg_max` segments (work units) per sequence.
 struct DecodeGeom {
     int cluster, chunk, nseg_max;
 };

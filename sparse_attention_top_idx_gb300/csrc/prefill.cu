@@ -1,6 +1,6 @@
 // prefill.cu -- causal-chunk scoring (tcgen05 kernel with 4 queries per CTA,
 // scores to the workspace) followed by the per-row exact top-k select.
-#include "score_kernel.cuh"
+#include "prefill_kernel.cuh"
 
 namespace dsaidx {
 
@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(kTopkThreads, 3) prefill_select_kernel(const S
     each([&](uint64_t c, bool v) { hist_add_warp(hist, key_bin(comp_key(c)), v); });
     __syncthreads();
     auto each_slow = [&](auto f) { walk_row_slow(row, nvis, f); };
-    select_topk_from_hist(each, each_slow, hist, p.topk, sel, IDX_MAX_TOPK + kSelBcap, ss, oi, os);
+    const int nout = block_topk_sorted(each, each_slow, hist, p.topk, sel, IDX_MAX_TOPK + kSelBcap, ss);
+    write_topk_row(sel, nout, p.topk, oi, os);
 }
 
 template <bool kFp8, int kBs>
@@ -76,7 +77,7 @@ cudaError_t launch_prefill_t(const idx_cache* c, const ScoreParams& p, cudaStrea
     static std::atomic<unsigned long long> attr_done{0};
     static std::atomic<unsigned long long> sel_attr_done{0};
     const SmemPlan plan = make_plan(kFp8, kPrefillQT, 0);
-    auto kern = score_kernel<kFp8, kBs, kPrefillQT>;
+    auto kern = prefill_score_kernel<kFp8, kBs>;
     cudaError_t e = set_smem_once(kern, plan.total, attr_done);
     if (e != cudaSuccess) return e;
     if (p.num_groups > 0) {

@@ -1,0 +1,491 @@
+// segsel.cuh -- exact top-k of one segment's scores held in shared memory, by
+// one 256-thread CTA (the decode leader), written for latency: every pass
+// reads four scores per 16-byte load with several loads in flight.
+//
+// The rule is the indexer's ("The Hypothesis That Refused to Die", section
+// "The Context": the k best-scoring positions), ties to the lower index.
+// Candidates are 64-bit composites (score key << 32) | ~index, so a larger
+// composite is a better candidate (common.cuh, topk.cuh).
+//
+//  1. key range: the smallest and largest score key of the segment;
+//  2. histogram: 4096 bins of the keys mapped onto the full 32 bits by
+//     (key - lo) << z (order-preserving; iid scores fill about one octave of
+//     the float format, where the plain top 12 bits would give a few bins);
+//  3. boundary: the bin holding the k-th largest mapped key;
+//  4. collect: every composite in a bin at or above the boundary (k plus the
+//     boundary bin's few extra entries) into a buffer, warp-aggregated;
+//  5. when the collected set is much larger than k (many equal or near-equal
+//     scores), refine the boundary bin by 8-bit digits of the composite;
+//  6. sort the collected composites (topk.cuh rank or counting sort) and map
+//     the winners' keys back.
+#pragma once
+
+#include "common.cuh"
+#include "topk.cuh"
+
+namespace dsaidx {
+
+struct SegSelSmem {
+    uint32_t red[16];
+    uint32_t wcnt[8];
+    Boundary bnd;
+    uint32_t scratch[256];
+};
+
+// Calls f(key, index, valid) for the n scores s[0, n) (16-byte aligned,
+// readable up to n rounded up to 4), index = base + position, with four loads
+// in flight per thread and warp-uniform trip counts.
+template <class F>
+__device__ __forceinline__ void seg_walk(const float* s, int n, int base, F f) {
+    const float4* s4 = reinterpret_cast<const float4*>(s);
+    const int nj = (n + 3) >> 2;
+    constexpr int U = 4;
+    for (int j0 = 0; j0 < nj; j0 += kTopkThreads * U) {
+        float4 x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * kTopkThreads + static_cast<int>(threadIdx.x);
+            x[u] = j < nj ? s4[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = 4 * (j0 + u * kTopkThreads + static_cast<int>(threadIdx.x));
+            f(score_key(x[u].x), base + i, i < n);
+            f(score_key(x[u].y), base + i + 1, i + 1 < n);
+            f(score_key(x[u].z), base + i + 2, i + 2 < n);
+            f(score_key(x[u].w), base + i + 3, i + 3 < n);
+        }
+    }
+}
+
+// Calls f(key, index, valid) for the n composites c[0, n) (16-byte aligned,
+// readable up to n rounded up to 2), two per load, four loads in flight.
+template <class F>
+__device__ __forceinline__ void comp_walk(const uint64_t* c, int n, F f) {
+    const uint4* c4 = reinterpret_cast<const uint4*>(c);
+    const int nj = (n + 1) >> 1;
+    constexpr int U = 4;
+    for (int j0 = 0; j0 < nj; j0 += kTopkThreads * U) {
+        uint4 x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * kTopkThreads + static_cast<int>(threadIdx.x);
+            x[u] = j < nj ? c4[j] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = 2 * (j0 + u * kTopkThreads + static_cast<int>(threadIdx.x));
+            f(x[u].y, static_cast<int32_t>(~x[u].x), i < n);
+            f(x[u].w, static_cast<int32_t>(~x[u].z), i + 1 < n);
+        }
+    }
+}
+
+// A segment of n scores in shared memory (key indices base + position).
+struct ScoreSet {
+    const float* s;
+    int n, base;
+    template <class F>
+    __device__ __forceinline__ void operator()(F f) const { seg_walk(s, n, base, f); }
+};
+// A segment of n scores in global memory written by other CTAs (read through
+// L2, not L1).  Like every walk here, the trip count is the same in all lanes
+// of a warp (callers may vote inside f).
+struct GScoreSet {
+    const float* s;
+    int n, base;
+    template <class F>
+    __device__ __forceinline__ void operator()(F f) const {
+        const float4* s4 = reinterpret_cast<const float4*>(s);
+        const int nj = (n + 3) >> 2;
+        for (int j0 = 0; j0 < nj; j0 += kTopkThreads) {
+            const int j = j0 + static_cast<int>(threadIdx.x);
+            const float4 x = j < nj ? __ldcg(s4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int i = 4 * j;
+            f(score_key(x.x), base + i, i < n);
+            f(score_key(x.y), base + i + 1, i + 1 < n);
+            f(score_key(x.z), base + i + 2, i + 2 < n);
+            f(score_key(x.w), base + i + 3, i + 3 < n);
+        }
+    }
+};
+// A set of n composites in global memory (read through L2).
+struct GCompSet {
+    const uint64_t* c;
+    int n;
+    template <class F>
+    __device__ __forceinline__ void operator()(F f) const {
+        const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(c);
+        const int nj = (n + 1) >> 1;
+        for (int j0 = 0; j0 < nj; j0 += kTopkThreads) {
+            const int j = j0 + static_cast<int>(threadIdx.x);
+            ulonglong2 x;
+            x.x = 0ull;
+            x.y = 0ull;
+            if (j < nj) x = __ldcg(c2 + j);
+            const int i = 2 * j;
+            f(static_cast<uint32_t>(x.x >> 32), comp_index(x.x), i < n && x.x != 0ull);
+            f(static_cast<uint32_t>(x.y >> 32), comp_index(x.y), i + 1 < n && x.y != 0ull);
+        }
+    }
+};
+// A set of n composites in shared memory.
+struct CompSet {
+    const uint64_t* c;
+    int n;
+    template <class F>
+    __device__ __forceinline__ void operator()(F f) const { comp_walk(c, n, f); }
+};
+
+// The exact top-k of a set (ScoreSet or CompSet, `walk`) into buf[0, nout)
+// sorted descending as composites of the ORIGINAL score keys; returns nout =
+// min(k, set size).  hist: 4096 words; buf: >= 4096 composites (collection
+// and sort scratch, disjoint from the set).  All 256 threads.
+template <class Set>
+__device__ __noinline__ int seg_select(const Set walk, int k, uint32_t* hist, uint64_t* buf, SegSelSmem* sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // 1. key range
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    for (int i = tid; i < kHistBins; i += kTopkThreads) hist[i] = 0u;
+    walk([&](uint32_t key, int, bool v) {
+        lo = v ? min(lo, key) : lo;
+        hi = v ? max(hi, key) : hi;
+    });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) {
+        sm->red[warp] = lo;
+        sm->red[8 + warp] = hi;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        lo = min(lo, sm->red[w]);
+        hi = max(hi, sm->red[8 + w]);
+    }
+    const int z = hi > lo ? __clz(hi - lo) : 0;
+    // 2. histogram of the mapped keys' top 12 bits
+    walk([&](uint32_t key, int, bool v) {
+        if (v) atomicAdd(&hist[((key - lo) << z) >> kHistShift], 1u);
+    });
+    __syncthreads();
+    // 3. boundary bin of the k-th largest
+    block_find_suffix(hist, kHistBins, static_cast<uint32_t>(k), sm->scratch, &sm->bnd);
+    const int bstar = sm->bnd.bin;   // -1: fewer than k scores, all are taken
+    const uint32_t bthr = bstar >= 0 ? static_cast<uint32_t>(bstar) : 0u;
+    // 4. collect the composites (mapped keys) in bins >= the boundary: each
+    //    warp appends to its own segment of buf[2048, 4096) with ballots,
+    //    then the segments are packed into buf[0, count)
+    constexpr int kSeg = 2048 / 8;
+    uint64_t* segs = buf + 2048;
+    uint32_t cnt = 0;   // this warp's, the same in every lane
+    walk([&](uint32_t key, int idx, bool v) {
+        const uint32_t m = (key - lo) << z;
+        const bool t = v && (m >> kHistShift) >= bthr;
+        const unsigned b = __ballot_sync(0xffffffffu, t);
+        if (t) {
+            const uint32_t p = cnt + static_cast<uint32_t>(__popc(b & ((1u << lane) - 1u)));
+            if (p < static_cast<uint32_t>(kSeg)) segs[warp * kSeg + p] = make_comp(m, idx);
+        }
+        cnt += static_cast<uint32_t>(__popc(b));
+    });
+    if (lane == 0) sm->wcnt[warp] = cnt;
+    __syncthreads();
+    uint32_t before = 0, count = 0;
+    bool over = false;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint32_t c = sm->wcnt[w];
+        before += w < warp ? c : 0u;
+        count += c;
+        over |= c > static_cast<uint32_t>(kSeg);
+    }
+    int nsort;
+    if (!over && count <= 2048u) {
+        for (uint32_t i = lane; i < cnt; i += 32) buf[before + i] = segs[warp * kSeg + i];
+        __syncthreads();
+        nsort = static_cast<int>(count);
+        if (bstar >= 0 && count > static_cast<uint32_t>(max(kTopkThreads, next_pow2(k)))) {
+            // 5. a crowded boundary bin: keep its best (k - above) by radix
+            //    passes over the collected list, then compact
+            const uint32_t above = sm->bnd.above;
+            const uint32_t m = static_cast<uint32_t>(k) - above;
+            auto each = [&](auto f) { walk_smem(buf, count, f); };
+            SelectSmem* ss = reinterpret_cast<SelectSmem*>(hist);   // the histogram is no longer needed
+            const uint64_t thr = radix_refine(each, bstar, m, ss);
+            nsort = static_cast<int>(block_collect(
+                each, [&](uint64_t c) { return static_cast<int>(comp_key(c) >> kHistShift) > bstar || c >= thr; },
+                segs, 2048u, sm->scratch));
+            for (int i = tid; i < nsort; i += kTopkThreads) buf[i] = segs[i];
+            __syncthreads();
+        }
+    } else {
+        // many equal or near-equal scores in the boundary bin (more than the
+        // buffer holds): refine the boundary bin over the whole segment, then
+        // collect exactly k
+        __syncthreads();
+        const uint32_t above = sm->bnd.above;
+        const uint32_t m = static_cast<uint32_t>(k) - above;
+        auto each_all = [&](auto f) {
+            walk([&](uint32_t key, int idx, bool v) { f(make_comp((key - lo) << z, idx), v); });
+        };
+        SelectSmem* ss = reinterpret_cast<SelectSmem*>(hist);
+        const uint64_t thr = radix_refine(each_all, bstar, m, ss);
+        nsort = static_cast<int>(block_collect(
+            each_all, [&](uint64_t c) { return static_cast<int>(comp_key(c) >> kHistShift) > bstar || c >= thr; },
+            buf, static_cast<uint32_t>(k), sm->scratch));
+        nsort = min(nsort, k);
+    }
+    // 6. sort, then map the keys back
+    block_sort_any(buf, nsort, buf + 2048);
+    const int nout = min(k, nsort);
+    for (int j = tid; j < nout; j += kTopkThreads) {
+        const uint64_t c = buf[j];
+        buf[j] = make_comp((comp_key(c) >> z) + lo, comp_index(c));
+    }
+    __syncthreads();
+    return nout;
+}
+
+
+// ---------------------------------------------------------------------------
+// Ordering a small candidate set without a comparison sort
+// ---------------------------------------------------------------------------
+
+// Sorts the n composites of a[0, n) descending, n <= 2048, leaving them in
+// a[0, n); every key lies in [lo, hi].  The keys are mapped onto 32 bits over
+// that range and a 4096-bin histogram gives each bin its first output place
+// (thread t holds bins 16 t .. 16 t + 15 in registers); every element is
+// scattered to its bin's next place in tmp and then placed by its rank inside
+// its bin (bins hold a few elements for spread keys).  A bin of more than 64
+// elements (many equal or very close keys) sends the set to the rank sort.
+// hist, cur: 4096 words each; tmp: n composites (disjoint from a).  All 256
+// threads.
+__device__ __noinline__ void bin_order(uint64_t* a, int n, uint64_t* tmp, uint32_t lo, uint32_t hi, uint32_t* hist,
+                                       uint32_t* cur, SegSelSmem* sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int z = hi > lo ? __clz(hi - lo) : 0;
+    auto bin_of = [&](uint64_t c) { return ((comp_key(c) - lo) << z) >> kHistShift; };
+    {
+        uint4* h4 = reinterpret_cast<uint4*>(hist);
+        for (int i = tid; i < kHistBins / 4; i += kTopkThreads) h4[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += kTopkThreads) atomicAdd(&hist[bin_of(a[i])], 1u);
+    __syncthreads();
+    // counts of this thread's 16 bins, their first places, the largest count
+    uint32_t v[16];
+    {
+        const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 4 * tid;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 x = h4[j];
+            v[4 * j] = x.x;
+            v[4 * j + 1] = x.y;
+            v[4 * j + 2] = x.z;
+            v[4 * j + 3] = x.w;
+        }
+    }
+    uint32_t sum = 0, mx = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        sum += v[j];
+        mx = max(mx, v[j]);
+    }
+    uint32_t incl = sum;   // over this warp's lanes >= lane (higher bins)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) {
+        sm->scratch[warp] = incl;
+        sm->scratch[8 + warp] = mx;
+    }
+    __syncthreads();
+    uint32_t after = incl - sum;
+    mx = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        after += q > warp ? sm->scratch[q] : 0u;
+        mx = max(mx, sm->scratch[8 + q]);
+    }
+    if (mx > 64u) {
+        block_sort_any(a, n, tmp);
+        return;
+    }
+    {
+        uint32_t st[16];
+        uint32_t acc = after;
+#pragma unroll
+        for (int j = 15; j >= 0; --j) {
+            st[j] = acc;
+            acc += v[j];
+        }
+        uint4* o4 = reinterpret_cast<uint4*>(hist) + 4 * tid;
+        uint4* c4 = reinterpret_cast<uint4*>(cur) + 4 * tid;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 x = make_uint4(st[4 * j], st[4 * j + 1], st[4 * j + 2], st[4 * j + 3]);
+            o4[j] = x;
+            c4[j] = x;
+        }
+    }
+    __syncthreads();
+    // scatter every element to its bin's next place
+    for (int i = tid; i < n; i += kTopkThreads) {
+        const uint64_t c = a[i];
+        tmp[atomicAdd(&cur[bin_of(c)], 1u)] = c;
+    }
+    __syncthreads();
+    // place every element by its rank inside its bin [hist[b], cur[b])
+    for (int i = tid; i < n; i += kTopkThreads) {
+        const uint64_t c = tmp[i];
+        const uint32_t b = bin_of(c);
+        const uint32_t e = cur[b];
+        uint32_t r = hist[b];
+        for (uint32_t j = r; j < e; ++j) r += tmp[j] > c ? 1u : 0u;
+        a[r] = c;
+    }
+    __syncthreads();
+}
+
+// Exact sorted top-k of the n composites c[0, n) (n <= 2048, in shared
+// memory): their key range, then bin_order; c[0, min(k, n)) then holds the
+// winners.  tmp: n composites; hist, cur: 4096 words.  All 256 threads.
+__device__ __noinline__ int small_select(uint64_t* c, int n, int k, uint64_t* tmp, uint32_t* hist, uint32_t* cur,
+                                         SegSelSmem* sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    for (int i = tid; i < n; i += kTopkThreads) {
+        const uint32_t key = comp_key(c[i]);
+        lo = min(lo, key);
+        hi = max(hi, key);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) {
+        sm->red[warp] = lo;
+        sm->red[8 + warp] = hi;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        lo = min(lo, sm->red[w]);
+        hi = max(hi, sm->red[8 + w]);
+    }
+    bin_order(c, n, tmp, lo, hi, hist, cur, sm);
+    return min(k, n);
+}
+
+// Histogram windows of the decode selection: bins of the score key at
+// 1/32 octave (key >> 19, 8192 bins over all keys); a CTA's window is the 256
+// bins below its largest score.
+constexpr int kWinShift = 19;
+constexpr int kWinBins = 256;                        // bins of a window, ending at the chunk's largest
+constexpr int kWinHead = 4;                          // anchor bin, count, largest key, device-check flag
+constexpr int kWinWords = kWinHead + kWinBins / 2;   // then 16-bit counts in pairs (528 bytes)
+constexpr int kCountSortMax = 96;                    // longest candidate list sorted by counting
+
+__device__ __forceinline__ uint32_t win_bin(uint32_t key) { return key >> kWinShift; }
+
+// Bins of the per-sequence histogram of the segments' runs: 1/32 octave.
+constexpr int kGHistBins = 8192;
+
+// Exact sorted top-k over the nseg sorted runs of k composites (zero-padded)
+// of one sequence, runs[j * k + e] in global memory, given the histogram gh
+// (kGHistBins bins of key >> 19) of every run entry: the boundary bin of the
+// k-th largest entry, then each run's prefix at or above it (runs are sorted,
+// so a warp reads a run 32 entries at a time until a read holds none) as the
+// candidates, ordered by small_select.  With more candidates than fit,
+// selects over all run entries (seg_select).  buf: >= 4096 composites; hist,
+// cur: 4096 words.  Returns nout, buf[0, nout) sorted descending.  All 256
+// threads.
+__device__ __noinline__ int merge_runs(const uint64_t* runs, int nseg, int k, const uint32_t* gh, uint32_t* hist,
+                                       uint32_t* cur, uint64_t* buf, SegSelSmem* sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // suffix find over the 8192 bins: thread t holds bins 32 t .. 32 t + 31
+    uint32_t v[32];
+    {
+        const uint4* g4 = reinterpret_cast<const uint4*>(gh) + 8 * tid;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 x = __ldcg(g4 + j);
+            v[4 * j] = x.x;
+            v[4 * j + 1] = x.y;
+            v[4 * j + 2] = x.z;
+            v[4 * j + 3] = x.w;
+        }
+    }
+    uint32_t sum = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) sum += v[j];
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+    }
+    if (lane == 0) sm->wcnt[warp] = incl;
+    if (tid == 0) {
+        sm->bnd.bin = -1;
+        sm->bnd.above = 0u;
+    }
+    __syncthreads();
+    uint32_t after = incl - sum, total = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint32_t x = sm->wcnt[q];
+        after += q > warp ? x : 0u;
+        total += x;
+    }
+    const uint32_t kk = min(static_cast<uint32_t>(k), total);
+    if (kk > 0u && after < kk && kk <= after + sum) {
+        uint32_t acc = after;
+#pragma unroll
+        for (int j = 31; j >= 0; --j) {
+            if (acc < kk && kk <= acc + v[j]) {
+                sm->bnd.bin = 32 * tid + j;
+                sm->bnd.above = acc + v[j];   // entries at or above the bin
+            }
+            acc += v[j];
+        }
+    }
+    __syncthreads();
+    const int bstar = sm->bnd.bin;
+    const uint32_t ncand = sm->bnd.above;
+    if (bstar < 0) return 0;
+    uint64_t* cand = buf + 2048;
+    if (ncand <= 2048u) {
+        // each run's prefix at or above the boundary bin, per warp into segments
+        // of the candidate buffer (two passes: count, then write at offsets)
+        auto walk = [&](auto f) {
+            for (int j = warp; j < nseg; j += kTopkThreads / 32) {
+                const unsigned long long* rr = reinterpret_cast<const unsigned long long*>(runs) + static_cast<int64_t>(j) * k;
+                for (int m = 0; m < k; m += 32) {
+                    const int e = m + lane;
+                    const uint64_t c = e < k ? static_cast<uint64_t>(__ldcg(rr + e)) : 0ull;
+                    const bool t = c != 0ull && static_cast<int>(win_bin(comp_key(c))) >= bstar;
+                    f(c, t);
+                    if (!__any_sync(0xffffffffu, t)) break;
+                }
+            }
+        };
+        const uint32_t got = block_collect(walk, [](uint64_t) { return true; }, cand, 2048u, sm->scratch);
+        const int nout = small_select(cand, static_cast<int>(min(got, 2048u)), k, buf, hist, cur, sm);
+        for (int i = tid; i < nout; i += kTopkThreads) buf[i] = cand[i];
+        __syncthreads();
+        return nout;
+    }
+    return seg_select(GCompSet{runs, nseg * k}, k, hist, buf, sm);
+}
+
+}  // namespace dsaidx

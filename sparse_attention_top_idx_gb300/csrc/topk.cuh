@@ -496,16 +496,17 @@ __device__ __forceinline__ int next_pow2(int x) {
     return p;
 }
 
-// Final selection of one query row from a candidate set whose 4096-bin
-// histogram `hist` (shared) is exact.  each(f) walks every candidate once
-// (the fast, unrolled walk: called at one place); each_slow(f) walks them
-// again with compact code, only when the boundary bin overflows shared
-// memory.  buf: shared buffer of cap >= 4096 composites: [0, 2048) collects
-// the selection, the rest first the boundary bin, then the sort's scratch.
-// Writes the k outputs (descending, -1 / -inf padded).  All 256 threads.
+// Exact top-k of one candidate set whose 4096-bin histogram `hist` (shared)
+// is exact for every candidate in the bins at and above the boundary.
+// each(f) walks every candidate once (the fast walk, called at one place);
+// each_slow(f) walks them again with compact code, only when the boundary bin
+// overflows shared memory.  buf: shared buffer of cap >= 4096 composites:
+// [0, 2048) collects the selection, the rest first the boundary bin, then the
+// sort's scratch.  On return buf[0, nout) holds the winners in descending
+// order (nout = min(k, candidates)).  All 256 threads.
 template <class Each, class EachSlow>
-__device__ void select_topk_from_hist(Each each, EachSlow each_slow, const uint32_t* hist, int k, uint64_t* buf,
-                                      int cap, SelectSmem* ss, int32_t* out_idx, float* out_score) {
+__device__ int block_topk_sorted(Each each, EachSlow each_slow, const uint32_t* hist, int k, uint64_t* buf, int cap,
+                                 SelectSmem* ss) {
     const int tid = threadIdx.x;
     block_find_suffix(hist, kHistBins, static_cast<uint32_t>(k), ss->scratch, &ss->bnd);
     const int bstar = ss->bnd.bin;
@@ -598,8 +599,14 @@ __device__ void select_topk_from_hist(Each each, EachSlow each_slow, const uint3
         __syncthreads();
     }
     block_sort_any(buf, nsort, bndbuf);
-    const int nout = min(k, nsort);
-    for (int j = tid; j < k; j += kTopkThreads) {
+    return min(k, nsort);
+}
+
+// Write a top-k row: buf[0, nout) as indices (and scores), the rest of the k
+// outputs as -1 (and -inf).  nout < 0 writes a whole -1 row.  All threads.
+__device__ __forceinline__ void write_topk_row(const uint64_t* buf, int nout, int k, int32_t* out_idx,
+                                               float* out_score) {
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
         if (j < nout) {
             const uint64_t c = buf[j];
             out_idx[j] = comp_index(c);

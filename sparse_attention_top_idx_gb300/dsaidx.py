@@ -70,6 +70,8 @@ def load(path: Optional[str] = None):
     L.idx_read_device_status.restype = I
     L.idx_status_str.argtypes = [I]
     L.idx_status_str.restype = ctypes.c_char_p
+    L.idx_test_set_wait_limit.argtypes = [ctypes.c_ulonglong]
+    L.idx_test_set_wait_limit.restype = I
     if path is None:
         _lib = L
     return L
@@ -257,3 +259,9 @@ def read_device_status(workspace: torch.Tensor, stream=None) -> int:
     _check(load().idx_read_device_status(_ptr(workspace), _stream(stream), ctypes.byref(v)),
            "idx_read_device_status")
     return int(v.value)
+
+
+def test_set_wait_limit(limit_ns: int = 0):
+    """idx_test_set_wait_limit: shorten the decode kernel's pipeline waits (and
+    withhold one MMA signal) so that the timeout path runs; 0 restores."""
+    _check(load().idx_test_set_wait_limit(int(limit_ns)), "idx_test_set_wait_limit")

@@ -16,7 +16,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = dsaidx.header_functions()
-    assert len(names) == 12, names
+    assert len(names) == 13, names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -51,5 +51,6 @@ def test_host_argument_checks(lib):
     assert lib.idx_workspace_init(None, 1024, None) == 1
     v = ctypes.c_int32()
     assert lib.idx_read_device_status(None, None, ctypes.byref(v)) == 1
+    assert lib.idx_test_set_wait_limit(0) == 0     # restores the normal limit
     assert dsaidx.status_str(0) == "ok"
     assert dsaidx.status_str(4) == "workspace too small"

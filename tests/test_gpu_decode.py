@@ -201,3 +201,22 @@ def test_workspace_too_small_is_rejected():
         dsaidx.score_topk_decode(cache, ins["q"], ins["w"], ins["block_table"], ins["seq_lens"], 300, 64,
                                  oi, ws)
     assert e.value.code == 4
+
+
+def test_timeout_path_flags_rows_and_the_next_call_recovers():
+    # The test hook shortens the pipeline waits to 2 ms and makes each CTA's
+    # MMA issuer withhold the signal of its first accumulator, so every CTA's
+    # epilogue wait runs out (no GPU fault, trap or hang: the wait is bounded).
+    # The call must record IDX_ERR_TIMEOUT, write -1 rows, drain its copies
+    # and MMAs and free TMEM; a normal call afterwards must pass parity.
+    W = wl.make_workload("tmo", [4500, 10000, 30000], [1, 1, 1], topk=512, seed=71)
+    cache = build_cache(W, dsaidx.FP8)
+    dsaidx.test_set_wait_limit(2_000_000)
+    try:
+        got = run_decode(W, dsaidx.FP8, cache=cache, expect_status=6)
+    finally:
+        dsaidx.test_set_wait_limit(0)
+    assert np.all(got["idx"] == -1)
+    assert np.all(np.isneginf(got["score"]))
+    again = run_decode(W, dsaidx.FP8, cache=cache)
+    check(W, dsaidx.FP8, again)

@@ -55,14 +55,20 @@ def test_static_scratch_decode_matches_workspace_decode(mode):
 
 
 def test_static_scratch_rejects_oversized_shape():
-    W = wl.make_workload("noalloc_big", [1000], [1], topk=64, seed=7)
+    W = wl.make_workload("noalloc_big", [1000], [1], topk=2048, seed=7)
     cache = build_cache(W, dsaidx.FP8)
     ins = decode_inputs(W)
-    oi = torch.empty((1, 64), dtype=torch.int32, device="cuda")
-    osc = torch.empty((1, 64), dtype=torch.float32, device="cuda")
+    oi = torch.empty((1, 2048), dtype=torch.int32, device="cuda")
+    osc = torch.empty((1, 2048), dtype=torch.float32, device="cuda")
+    # a bound of 128M keys with top-2048 needs per sequence a sorted top-k run
+    # for each of its 2048 segments of 65536 keys (32 MiB) besides the slow-path
+    # scratch: more than the 32 MiB area, so the call is refused before
+    # anything is launched
+    need = dsaidx.workspace_bytes_decode(cache, 1, 1 << 27, 64, 2048)
+    assert need > 32 << 20
     big = dsaidx.load().idx_score_topk_decode_static(
         cache.handle, ctypes.c_void_p(ins["q"].data_ptr()), ctypes.c_void_p(ins["w"].data_ptr()),
         ctypes.c_void_p(ins["block_table"].data_ptr()), ins["block_table"].shape[1],
-        ctypes.c_void_p(ins["seq_lens"].data_ptr()), 1, 4 << 20, 64, 64,
+        ctypes.c_void_p(ins["seq_lens"].data_ptr()), 1, 1 << 27, 64, 2048,
         ctypes.c_void_p(oi.data_ptr()), ctypes.c_void_p(osc.data_ptr()), None)
-    assert big == 4     # IDX_ERR_WORKSPACE_TOO_SMALL: 4M keys need more than the 8 MiB area
+    assert big == 4     # IDX_ERR_WORKSPACE_TOO_SMALL
