@@ -69,7 +69,7 @@ DecodeWs decode_ws(const idx_cache* c, int batch, int max_seq_len, int topk) {
     w.seqflag = o;  o = align_up(o + nb * 4, 256);
     w.ucount = o;   o = align_up(o + 8, 256);
     w.scratch = o;  o = align_up(o + clusters * dsaidx::kDecCl * static_cast<size_t>(w.geom.chunk) * 4, 256);
-    w.ghist = o;    o = align_up(o + (multi ? nb * 8192 * 4 : 0), 256);
+    w.ghist = o;    o = align_up(o + (multi ? nb * dsaidx::kGHistWords * 4 : 0), 256);
     w.runs = o;     o = align_up(o + nb * static_cast<size_t>(w.runs_cap) * 8, 256);
     w.total = o;
     return w;

@@ -289,6 +289,16 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
+// Bulk copy from this CTA's shared memory to another CTA's (dst and bar are
+// shared::cluster addresses in the receiving CTA); the bytes are counted on
+// the receiver's mbarrier.  16-byte aligned addresses, size a multiple of 16.
+// The sender's generic writes of the source need fence.proxy.async first.
+__device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
 // L2 eviction policies for the cache hints.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

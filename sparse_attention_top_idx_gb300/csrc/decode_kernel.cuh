@@ -19,14 +19,18 @@
 // cluster is launched idle and clusters that start late find less work.
 //
 // One unit, in every CTA of the cluster (warp roles):
-//   warp 0     lane 0 starts the copy of the sequence's 64 bf16 query rows and
-//              head weights, the warp loads the chunk's block ids, then lane 0
-//              issues one TMA box per paged block (64 or 32 rows of 128 bytes,
-//              128-byte swizzle) into a ring of stages;
+//   warp 0     lane 0 starts the copy of this CTA's 8 of the sequence's 64
+//              bf16 query rows and their head weights, the warp loads the
+//              chunk's block ids, then lane 0 issues one TMA box per paged
+//              block (64 or 32 rows of 128 bytes, 128-byte swizzle) into a
+//              ring of stages;
 //   warp 1     owns TMEM; lane 0 issues tcgen05.mma (M = 128 keys, N = 64
 //              heads, K = 128) into a double-buffered fp32 accumulator;
-//   warps 2-5  quantise the 64 query rows into the B operand, two lanes per
-//              row (each CTA builds its own copy: no exchange);
+//   warps 2-5  quantise this CTA's 8 query rows into its 1 KB block of the B
+//              operand (16 lanes per row) and send the block and the rows'
+//              w' to the other 7 CTAs (bulk shared-to-shared copies counted
+//              on their query barrier), so the B tile is built once per
+//              cluster;
 //   warps 4-7  run the epilogue: one key row per thread, 16 TMEM columns at a
 //              time, ks[s] * sum_h w'[h] * max(D, 0) with the head weights in
 //              registers and the key scale loaded from the cache two tiles
@@ -37,21 +41,24 @@
 // a round trip):
 //   1. every CTA sends every CTA its window: the 256 histogram bins below its
 //      largest score, its key count and largest key (528 bytes);
-//   2. every CTA sums the windows: the bin of the segment's k-th largest
-//      score and, from the windows, each CTA's number of candidates (scores
-//      in bins at or above it: about k plus the boundary bin) and offset;
-//   3. every CTA collects its candidates (a float comparison), sorts them and
-//      sends the sorted list to every CTA at its offset;
-//   4. every CTA ranks its own candidates by binary searches in the other
-//      lists and writes those of rank < k to the output (or the segment's
-//      run).
+//   2. every CTA sums the windows over the 256 bins below the segment's
+//      largest: the bin of the segment's k-th largest score (the boundary)
+//      and, per bin at or above it, every CTA's count, so the place of each
+//      bin's entries in a bin-major pool (bins from the top, CTAs in rank
+//      order within a bin) is known to every CTA;
+//   3. every CTA writes each of its candidates (scores in bins at or above
+//      the boundary) to its place in every CTA's pool: nothing is sorted;
+//   4. every CTA ranks one eighth of the pool -- the entries of higher bins
+//      plus the larger entries of the same bin -- and writes those of rank
+//      < k to the output (or the segment's run).
 // A crowded boundary bin (many equal or nearly equal scores) takes a slower
 // path: the chunks' scores go through a per-cluster global scratch to one
 // CTA, which selects with radix refinement (segsel.cuh).  A sequence longer
 // than one segment writes each segment's sorted top-k as a run and its bin
-// counts to the sequence's histogram in the workspace; the CTA that ends the
-// sequence's last segment (a ticket) merges: the histogram gives the boundary
-// bin and, runs being sorted, only each run's prefix at or above it is read.
+// counts (and largest bin) to the sequence's histogram in the workspace; the
+// CTA that ends the sequence's last segment (a ticket) merges: the histogram
+// gives the boundary bin and, runs being sorted, only each run's prefix at or
+// above it is read.
 //
 // Every mbarrier wait is bounded (%globaltimer); a wait that runs out sets
 // IDX_ERR_TIMEOUT, the CTA stops streaming (draining its copies and MMAs),
@@ -89,6 +96,11 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
     constexpr int kKSteps = kFp8 ? 4 : 8;                 // K = 128 in steps of 32 bytes
     constexpr uint32_t kBoxBytes = kBs * 128;             // one TMA box: a block's code rows (or half rows)
     constexpr int kQuantThreads = kThreads - 64;          // warps 2..7 take part in the query stage
+    constexpr int kQRows = kN / kDecCl;                   // query rows each CTA quantises
+    // bytes each other CTA sends: its rows' block of the B tile (each K-half
+    // for bf16) and their w'
+    constexpr uint32_t kQPushBytes = kQRows * 128 * (kFp8 ? 1 : 2) + kQRows * 4;
+    static_assert(kQRows == 8, "one 8-row swizzle atom (1 KB) of the B tile per CTA");
     constexpr int kEpiWarps = 4;
     constexpr uint32_t kWinBytes = kWinWords * 4;
 
@@ -99,11 +111,11 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
     const int kStages = plan.stages;
     uint8_t* a_tiles = smem + plan.a_off;
     uint8_t* raw = smem + plan.raw_off;                                 // staged bf16 query rows
-    float* wraw = reinterpret_cast<float*>(raw + kN * kHeadDim * 2);
+    float* wraw = reinterpret_cast<float*>(raw + kQRows * kHeadDim * 2);
     uint32_t* chist = reinterpret_cast<uint32_t*>(raw);                 // the chunk's 16-bit histogram (aliased)
     float* csc = reinterpret_cast<float*>(smem + plan.sc_off);          // this chunk's scores
     uint32_t* win = reinterpret_cast<uint32_t*>(smem + plan.win_off);   // [kDecCl][kWinWords]
-    uint64_t* pool = reinterpret_cast<uint64_t*>(smem + plan.pool_off); // every CTA's sorted candidates
+    uint64_t* pool = reinterpret_cast<uint64_t*>(smem + plan.pool_off); // the cluster's candidates, bin-major
     uint8_t* qtile = smem + plan.q_off;
     float* wq = reinterpret_cast<float*>(smem + plan.w_off);
     int* bids = reinterpret_cast<int*>(smem + plan.bid_off);
@@ -117,12 +129,10 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
     uint64_t* qbar = bars + 13;       // query rows and weights staged
     uint64_t* qready = bars + 14;     // B tile and w' written (one arrive per query-stage warp)
     uint64_t* wbar = bars + 15;       // every other CTA's window has arrived
-    uint64_t* lbar = bars + 16;       // every other CTA's sorted candidates have arrived
+    uint64_t* lbar = bars + 16;       // every other CTA's candidates have arrived
     uint64_t* ubar = bars + 17;       // [2] the next unit has arrived
     uint64_t* rbar = bars + 19;       // coordinating CTA: every CTA wrote its part of the unit
-    // after the stream the key stages hold the selection's lists and scratch
-    uint64_t* mine = reinterpret_cast<uint64_t*>(a_tiles);              // [2048] own candidates
-    uint64_t* sorted = mine + 2048;                                     // [2048] sort output
+    // after the stream the key stages hold the selection's tables and scratch
     // (slow path, merge: the chunk's scores are in global scratch or done with)
     uint32_t* shist = reinterpret_cast<uint32_t*>(csc);                 // [4096] selection histogram
     uint64_t* sbuf = reinterpret_cast<uint64_t*>(a_tiles);              // [4096] selection buffer
@@ -139,7 +149,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
     if (warp == 0) {
         if (lane == 0) {
             mbar_init(qbar, 1);
-            mbar_init(qready, kQuantThreads / 32);
+            mbar_init(qready, kQuantThreads / 32 + 1);   // + the arrival that expects the other CTAs' rows
             mbar_init(wbar, 1);
             mbar_init(lbar, 1);
             mbar_init(&ubar[0], 1);
@@ -166,6 +176,10 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
         tmem_alloc(&ks->tmem_base, 2 * kN);
         tmem_relinquish();
     }
+    // every CTA's barriers are initialised before any CTA sends it anything
+    // (the first unit's query rows): a whole-cluster barrier, its wait after
+    // the scan below
+    cluster_arrive();
     // units per sequence, scanned over the block: thread t holds sequences
     // [t * per, t * per + per) and the exclusive prefix of their units; with
     // one sequence per thread it keeps that sequence's length
@@ -196,7 +210,8 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
         total += t;
     }
     const uint32_t tmem = ks->tmem_base;
-    // every CTA's barriers are initialised before any CTA sends it anything
+    cluster_wait();
+    // the first half of the per-unit barrier (its wait follows the stream)
     cluster_arrive();
 
     uint32_t tcnt = 0;   // tiles streamed by this CTA so far (stage, phase and accumulator)
@@ -244,26 +259,30 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
         const int lb0 = key_begin / kBs;
         const uint32_t lead = static_cast<uint32_t>(u % kDecCl);   // the unit's coordinating CTA
 
-        if (run) {
+        if (live) {
             if (warp == 0) {
                 if (lane == 0) {
                     ks->bad = 0;
-                    const uint64_t pol_q = policy_evict_last();   // every CTA of the cluster reads it
-                    mbar_arrive_expect_tx(qbar, kN * kHeadDim * 2 + kN * 4);
-                    bulk_load(raw, p.q + static_cast<int64_t>(b) * kN * kHeadDim, kN * kHeadDim * 2, qbar, pol_q);
-                    bulk_load(wraw, p.w + static_cast<int64_t>(b) * kN, kN * 4, qbar, pol_q);
+                    // this CTA's query rows (the other CTAs send the rest of the B tile)
+                    const uint64_t pol_q = policy_evict_last();   // other clusters may read them too
+                    const int64_t row0 = static_cast<int64_t>(b) * kN + static_cast<int64_t>(rank) * kQRows;
+                    mbar_arrive_expect_tx(qbar, kQRows * kHeadDim * 2 + kQRows * 4);
+                    bulk_load(raw, p.q + row0 * kHeadDim, kQRows * kHeadDim * 2, qbar, pol_q);
+                    bulk_load(wraw, p.w + row0, kQRows * 4, qbar, pol_q);
                 }
                 // the chunk's block ids (a chunk spans at most kDecChunkMax / 32 blocks)
                 const int nblk = (key_end + kBs - 1) / kBs - lb0;
                 const int* bt_row = p.block_table + static_cast<int64_t>(b) * p.mbps;
-                for (int i = lane; i < nblk; i += 32) bids[i] = (lb0 + i < p.mbps) ? __ldg(bt_row + lb0 + i) : -1;
-                __syncwarp();
-                // hand the ids to the epilogue warps (their key-scale loads)
-                asm volatile("bar.arrive 2, %0;" ::"r"(32 + 32 * kEpiWarps) : "memory");
-                if (lane == 0) {
+                if (run) {
+                    for (int i = lane; i < nblk; i += 32) bids[i] = (lb0 + i < p.mbps) ? __ldg(bt_row + lb0 + i) : -1;
+                    __syncwarp();
+                    // hand the ids to the epilogue warps (their key-scale loads)
+                    asm volatile("bar.arrive 2, %0;" ::"r"(32 + 32 * kEpiWarps) : "memory");
+                }
+                if (run && lane == 0) {
                     // the key stream starts once the query rows have landed: issued
-                    // together, the whole grid's first key tiles (about 12 MB) would
-                    // queue ahead of the 16 KB query copy and hold up the MMAs
+                    // together, the whole grid's first key tiles (several MB) would
+                    // queue ahead of the query copies and hold up the MMAs
                     mbar_wait(qbar, qcnt & 1u, status, &ks->abort, wlim);
                     const uint64_t pol = policy_evict_first();
                     uint32_t T = issued;
@@ -309,7 +328,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                 }
                 issued = __shfl_sync(0xffffffffu, issued, 0);
             } else if (warp == 1) {
-                if (lane == 0) {
+                if (run && lane == 0) {
                     constexpr uint32_t idesc = idesc_make(kFp8, kTileKeys, kN);
                     const uint32_t q_base = smem_u32(qtile);
                     if (mbar_wait(qready, qcnt & 1u, status, &ks->abort, wlim)) {
@@ -345,22 +364,35 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                 }
                 __syncwarp();
             } else {
-                // warps 2..5: the B tile, two lanes per head row (one pass)
+                // warps 2..5: this CTA's 8 rows of the B tile, 16 lanes per row,
+                // then the rows' block and w' to the other CTAs
                 if (warp < 6) {
+                    if (tid == 64) mbar_arrive_expect_tx(qready, (kDecCl - 1) * kQPushBytes);
                     const bool have = __all_sync(0xffffffffu, mbar_wait(qbar, qcnt & 1u, status, &ks->abort, wlim));
+                    const int rl = (tid - 64) >> 4, part = tid & 15;
+                    const int r = static_cast<int>(rank) * kQRows + rl;
                     if (have) {
-                        const int r = (tid - 64) >> 1, h = tid & 1;
-                        const float wn = quant_row_half<kFp8>(raw + static_cast<size_t>(r) * kHeadDim * 2, h, wraw[r],
-                                                              0x3u << (lane & 30), qtile, r, kN);
-                        if (h == 0) wq[r] = wn;
+                        const float wn = quant_row_sixteenth<kFp8>(raw + static_cast<size_t>(rl) * kHeadDim * 2, part,
+                                                                   wraw[rl], 0xffffffffu, qtile, r, kN);
+                        if (part == 0) wq[r] = wn;
+                    }
+                    // the rows' bytes are visible to the copies and to this CTA's MMAs
+                    fence_proxy_async_smem();
+                    asm volatile("bar.sync 4, 128;" ::: "memory");
+                    if (warp == 2 && lane < kDecCl - 1 && have) {
+                        const uint32_t dst = static_cast<uint32_t>(lane) + (static_cast<uint32_t>(lane) >= rank ? 1u : 0u);
+                        const uint32_t bar = dsmem_addr(qready, dst);
+                        uint8_t* blk = qtile + rank * 1024u;
+                        bulk_copy_to_cta(dsmem_addr(blk, dst), blk, 1024u, bar);
+                        if constexpr (!kFp8) bulk_copy_to_cta(dsmem_addr(blk + kN * 128, dst), blk + kN * 128, 1024u, bar);
+                        bulk_copy_to_cta(dsmem_addr(wq + rank * kQRows, dst), wq + rank * kQRows, kQRows * 4u, bar);
                     }
                 }
-                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qready);
-                // every row's w' is written and the staged rows are consumed
+                // the staged rows are consumed (the histogram takes their place)
                 asm volatile("bar.sync 3, %0;" ::"r"(kQuantThreads) : "memory");
-                if (warp >= 4) {
+                if (warp >= 4 && run) {
                     // epilogue; first the chunk histogram (where the query rows were) is cleared
                     {
                         uint4* h4 = reinterpret_cast<uint4*>(chist);
@@ -371,6 +403,8 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                     const int qd = warp & 3;
                     const int row = qd * 32 + lane;
                     const uint32_t lane_base = tmem + (static_cast<uint32_t>(qd * 32) << 16);
+                    // every CTA's w' has arrived (the MMA waits on the same phase)
+                    const bool qok = __all_sync(0xffffffffu, mbar_wait(qready, qcnt & 1u, status, &ks->abort, wlim));
                     unsigned long long wr[32];
                     const unsigned long long* wq2 = reinterpret_cast<const unsigned long long*>(wq);
 #pragma unroll
@@ -390,7 +424,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                     };
                     float sc0 = scale_of(0), sc1 = scale_of(1);
                     uint32_t kmax = 0u;
-                    for (int t = 0; t < ntiles; ++t) {
+                    for (int t = 0; qok && t < ntiles; ++t) {
                         const uint32_t T = tcnt + static_cast<uint32_t>(t);
                         const int a = static_cast<int>(T & 1u);
                         const uint32_t aph = (T >> 1) & 1u;
@@ -433,7 +467,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                 }
             }
             ++qcnt;
-            tcnt += static_cast<uint32_t>(ntiles);
+            if (run) tcnt += static_cast<uint32_t>(ntiles);
         }
         __syncthreads();
         // a wait gave up during this unit: let every copy and MMA this CTA
@@ -584,14 +618,11 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
             }
             __syncthreads();
             bool fast = wtotal >= kk && bstar >= 0;
-            int ctot = 0, myoff = 0;
-            int offs[kDecCl];
+            int ctot = 0;
 #pragma unroll
             for (int r = 0; r < kDecCl; ++r) {
                 const int c = ks->cnt[r];
                 if (c < 0) fast = false;
-                offs[r] = ctot;
-                if (r < static_cast<int>(rank)) myoff += max(c, 0);
                 ctot += max(c, 0);
             }
             if (ctot > 2048 || ctot < nsel) fast = false;
@@ -601,105 +632,78 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
             int32_t* oi = p.out_idx + static_cast<int64_t>(b) * k;
             float* os = p.out_score ? p.out_score + static_cast<int64_t>(b) * k : nullptr;
             uint64_t* run_out = single ? nullptr : p.cand + static_cast<int64_t>(b) * p.cand_cap + static_cast<int64_t>(seg) * k;
-            uint32_t* gh = single ? nullptr : p.ghist + static_cast<int64_t>(b) * kGHistBins;
+            uint32_t* gh = single ? nullptr : p.ghist + static_cast<int64_t>(b) * kGHistWords;
             auto emit = [&](int r, uint64_t c) {
                 if (single) {
                     oi[r] = comp_index(c);
                     if (os) os[r] = key_score(comp_key(c));
                 } else {
                     run_out[r] = c;
-                    atomicAdd(gh + win_bin(comp_key(c)), 1u);
+                    const uint32_t wb = win_bin(comp_key(c));
+                    atomicAdd(gh + wb, 1u);
+                    if (r == 0) atomicMax(gh + kGHistBins, wb + 1u);   // the sequence's largest bin (+1)
                 }
             };
             if (flag) {
                 // a block id failed its check or a wait gave up: no selection
             } else if (fast) {
-                // ------------------------------------ 3. own candidates, sorted, to every CTA
-                const float fthr = key_score(static_cast<uint32_t>(bstar) << kWinShift);
+                // ------------------------------------ 3. the pool, in every CTA: the
+                // candidates (bins at or above the boundary) bin by bin from the top,
+                // within a bin CTA by CTA; each CTA writes its own to their places
+                // in every pool, so no CTA sorts anything
+                const int wlo = static_cast<int>(gmax) - (kWinBins - 1);   // bin of thread 0
+                uint32_t* bstart = reinterpret_cast<uint32_t*>(a_tiles);     // [kWinBins] first place of a bin
+                uint32_t* blen = bstart + kWinBins;                          // [kWinBins] its entries
+                uint32_t* bfill = blen + kWinBins;                           // [kWinBins] this CTA's next place
                 {
+                    uint32_t before = 0u;
+#pragma unroll
+                    for (int r = 0; r < kDecCl; ++r) before += r < static_cast<int>(rank) ? cr[r] : 0u;
+                    bstart[tid] = after;
+                    blen[tid] = hsum;
+                    bfill[tid] = after + before;
+                }
+                if (tid == 0) mbar_arrive_expect_tx(lbar, static_cast<uint32_t>(ctot - mycnt) * 8u);
+                __syncthreads();
+                {
+                    const uint32_t kthr = static_cast<uint32_t>(bstar) << kWinShift;   // smallest key of the boundary bin
                     const float4* s4 = reinterpret_cast<const float4*>(csc);
                     const int nj = (nkeys + 3) >> 2;
-                    uint32_t m = 0;
+                    auto place = [&](float v, int i) {
+                        const uint32_t key = score_key(v);
+                        if (i < nkeys && key >= kthr) {
+                            const uint64_t c = make_comp(key, key_begin + i);
+                            const uint32_t slot = atomicAdd(&bfill[static_cast<int>(win_bin(key)) - wlo], 1u);
+                            pool[slot] = c;
+#pragma unroll 1
+                            for (int q = 0; q < kDecCl - 1; ++q) {
+                                const uint32_t dst = static_cast<uint32_t>(q) + (static_cast<uint32_t>(q) >= rank ? 1u : 0u);
+                                dsmem_st_async_u64(dsmem_addr(pool + slot, dst), c, dsmem_addr(lbar, dst));
+                            }
+                        }
+                    };
                     for (int j = tid; j < nj; j += kThreads) {
                         const float4 x = s4[j];
-                        const int i = 4 * j;
-                        m += (x.x >= fthr) + (x.y >= fthr && i + 1 < nkeys) + (x.z >= fthr && i + 2 < nkeys) +
-                             (x.w >= fthr && i + 3 < nkeys);
+                        place(x.x, 4 * j);
+                        place(x.y, 4 * j + 1);
+                        place(x.z, 4 * j + 2);
+                        place(x.w, 4 * j + 3);
                     }
-                    uint32_t inc = m;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
-                        if (lane >= o) inc += y;
-                    }
-                    if (lane == 31) ks->scan[warp] = inc;
-                    __syncthreads();
-                    uint32_t pos = inc - m;
-                    for (int q = 0; q < warp; ++q) pos += ks->scan[q];
-                    if (m > 0u) {
-                        for (int j = tid; j < nj; j += kThreads) {
-                            const float4 x = s4[j];
-                            const int i = 4 * j;
-                            const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if (xs[e] >= fthr && i + e < nkeys && pos < 2048u)
-                                    mine[pos++] = make_comp(score_key(xs[e]), key_begin + i + e);
-                        }
-                    }
-                    __syncthreads();
-                }
-                // sorted (short lists by counting, longer ones by the rank sort)
-                uint64_t* mysorted;
-                if (mycnt <= kCountSortMax) {
-                    block_count_sort(mine, mycnt, sorted);
-                    mysorted = sorted;
-                } else {
-                    block_sort_any(mine, mycnt, sorted);
-                    mysorted = mine;
-                }
-                // to every CTA's pool at this CTA's offset (the own copy written here)
-                if (tid == 0) mbar_arrive_expect_tx(lbar, static_cast<uint32_t>(ctot - mycnt) * 8u);
-                for (int j = tid; j < mycnt; j += kThreads) pool[myoff + j] = mysorted[j];
-                for (int j = tid; j < mycnt * (kDecCl - 1); j += kThreads) {
-                    const int q = j / mycnt, e = j - q * mycnt;
-                    const uint32_t dst = static_cast<uint32_t>(q) + (static_cast<uint32_t>(q) >= rank ? 1u : 0u);
-                    dsmem_st_async_u64(dsmem_addr(pool + myoff + e, dst), mysorted[e], dsmem_addr(lbar, dst));
                 }
                 const bool lok = __syncthreads_and(mbar_wait_cluster(lbar, lcnt & 1u, status, 2 * kWaitLimitNs));
                 ++lcnt;
                 if (lok) {
-                    // ------------------------------------ 4. rank own candidates: the
-                    // larger members of every other list, by binary searches advanced
-                    // together
-                    int maxlen = 0;
-#pragma unroll
-                    for (int r = 0; r < kDecCl; ++r) maxlen = max(maxlen, ks->cnt[r]);
-                    const int steps = 32 - __clz(maxlen);
-                    int lens[kDecCl];
-#pragma unroll
-                    for (int r = 0; r < kDecCl; ++r) lens[r] = r == static_cast<int>(rank) ? 0 : max(ks->cnt[r], 0);
-                    for (int i = tid; i < mycnt; i += kThreads) {
-                        const uint64_t x = pool[myoff + i];
-                        int lo[kDecCl], ln[kDecCl];
-#pragma unroll
-                        for (int r = 0; r < kDecCl; ++r) {
-                            lo[r] = 0;
-                            ln[r] = lens[r];
-                        }
-                        for (int st = 0; st < steps; ++st) {
-#pragma unroll
-                            for (int r = 0; r < kDecCl; ++r) {
-                                const int half = ln[r] >> 1;
-                                const uint64_t y = pool[min(offs[r] + lo[r] + half, 2047)];
-                                const bool gt = ln[r] > 0 && y > x;
-                                lo[r] = gt ? lo[r] + half + 1 : lo[r];
-                                ln[r] = gt ? ln[r] - half - 1 : half;
-                            }
-                        }
-                        int rk = i;
-#pragma unroll
-                        for (int r = 0; r < kDecCl; ++r) rk += lo[r];
+                    // ------------------------------------ 4. this CTA's eighth of the
+                    // pool: rank = the entries of higher bins plus the larger entries
+                    // of its own bin
+                    const int lo = static_cast<int>(rank) * ctot / kDecCl;
+                    const int hi = (static_cast<int>(rank) + 1) * ctot / kDecCl;
+                    for (int i = lo + tid; i < hi; i += kThreads) {
+                        const uint64_t x = pool[i];
+                        const int t = static_cast<int>(win_bin(comp_key(x))) - wlo;
+                        const int s0 = static_cast<int>(bstart[t]), e0 = s0 + static_cast<int>(blen[t]);
+                        int rk = s0;
+                        for (int j = s0; j < e0; ++j) rk += pool[j] > x ? 1 : 0;
                         if (rk < nsel) emit(rk, x);
                     }
                 } else {
@@ -770,7 +774,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                                               reinterpret_cast<uint32_t*>(pool), sbuf, &ks->sel);
                         write_topk_row(sbuf, mout, k, oi, os);
                         // leave the sequence's workspace zeroed for the next call
-                        for (int i = tid; i < kGHistBins; i += kThreads) gh[i] = 0u;
+                        for (int i = tid; i < kGHistWords; i += kThreads) gh[i] = 0u;
                         if (tid == 0) {
                             p.ctr[b] = 0u;
                             p.seqflag[b] = 0u;

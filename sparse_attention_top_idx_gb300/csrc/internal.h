@@ -54,7 +54,7 @@ struct ScoreParams {
     // workspace
     int32_t* status;
     uint32_t* ctr;               // decode: [batch] completed-segment tickets
-    uint32_t* ghist;             // decode: [batch, 8192] bin counts of the segments' runs
+    uint32_t* ghist;             // decode: [batch, kGHistWords] bin counts of the segments' runs
     uint32_t* seqflag;           // decode: [batch] a segment failed a device check
     uint64_t* cand;              // decode: [batch, cand_cap] the segments' sorted top-k runs
     int64_t cand_cap;            // decode: nseg_max * topk composites per sequence
@@ -72,6 +72,10 @@ struct ScoreParams {
 // ---------------------------------------------------------------------------
 constexpr int kDecCl = 8;               // CTAs per cluster (one sequence segment)
 constexpr int kDecChunkMax = 8192;      // keys one CTA scores per segment
+// Per-sequence histogram of the segments' runs (score key >> 19); word
+// kGHistBins holds the largest bin of any run entry plus one (0: none).
+constexpr int kGHistBins = 8192;
+constexpr int kGHistWords = kGHistBins + 32;
 
 // Keys per CTA for a sequence of S > 0 keys: its share of a cluster rounded up
 // to the 128-key tile, at most kDecChunkMax.

@@ -1,12 +1,13 @@
-// segsel.cuh -- exact top-k of one segment's scores held in shared memory, by
-// one 256-thread CTA (the decode leader), written for latency: every pass
-// reads four scores per 16-byte load with several loads in flight.
+// segsel.cuh -- exact top-k building blocks of the decode selection, by one
+// 256-thread CTA, written for latency: every pass over scores reads four per
+// 16-byte load with several loads in flight.
 //
 // The rule is the indexer's ("The Hypothesis That Refused to Die", section
 // "The Context": the k best-scoring positions), ties to the lower index.
 // Candidates are 64-bit composites (score key << 32) | ~index, so a larger
 // composite is a better candidate (common.cuh, topk.cuh).
 //
+// seg_select (a segment's scores in global scratch, the crowded case):
 //  1. key range: the smallest and largest score key of the segment;
 //  2. histogram: 4096 bins of the keys mapped onto the full 32 bits by
 //     (key - lo) << z (order-preserving; iid scores fill about one octave of
@@ -16,8 +17,10 @@
 //     boundary bin's few extra entries) into a buffer, warp-aggregated;
 //  5. when the collected set is much larger than k (many equal or near-equal
 //     scores), refine the boundary bin by 8-bit digits of the composite;
-//  6. sort the collected composites (topk.cuh rank or counting sort) and map
-//     the winners' keys back.
+//  6. sort the collected composites and map the winners' keys back.
+// bin_order / small_select: a sorted order of at most 2048 composites by
+// mapped bins and ranks inside a bin.  merge_runs: the top-k of a long
+// sequence from its segments' sorted runs.
 #pragma once
 
 #include "common.cuh"
@@ -397,93 +400,172 @@ constexpr int kCountSortMax = 96;                    // longest candidate list s
 
 __device__ __forceinline__ uint32_t win_bin(uint32_t key) { return key >> kWinShift; }
 
-// Bins of the per-sequence histogram of the segments' runs: 1/32 octave.
-constexpr int kGHistBins = 8192;
 
 // Exact sorted top-k over the nseg sorted runs of k composites (zero-padded)
 // of one sequence, runs[j * k + e] in global memory, given the histogram gh
-// (kGHistBins bins of key >> 19) of every run entry: the boundary bin of the
-// k-th largest entry, then each run's prefix at or above it (runs are sorted,
-// so a warp reads a run 32 entries at a time until a read holds none) as the
-// candidates, ordered by small_select.  With more candidates than fit,
-// selects over all run entries (seg_select).  buf: >= 4096 composites; hist,
-// cur: 4096 words.  Returns nout, buf[0, nout) sorted descending.  All 256
-// threads.
+// (kGHistWords words: kGHistBins bins of key >> 19 over every run entry, then
+// the largest bin + 1).  The boundary bin of the k-th largest entry comes from
+// the 256 bins below the largest (all 8192 bins when those hold fewer than k);
+// the candidates are each run's prefix at or above it (runs are sorted), read
+// in rounds: every open run's next R entries, R sized so that a round is about
+// 1024 loads over the block, a run staying open while its last read entry is a
+// candidate; bin_order sorts them over the key range the histogram gives.
+// With more than 2048 candidates, selects over all run entries (seg_select).
+// buf: >= 4096 composites; hist, cur: 4096 words.  Returns nout, buf[0, nout)
+// sorted descending.  All 256 threads.
 __device__ __noinline__ int merge_runs(const uint64_t* runs, int nseg, int k, const uint32_t* gh, uint32_t* hist,
                                        uint32_t* cur, uint64_t* buf, SegSelSmem* sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // suffix find over the 8192 bins: thread t holds bins 32 t .. 32 t + 31
-    uint32_t v[32];
-    {
-        const uint4* g4 = reinterpret_cast<const uint4*>(gh) + 8 * tid;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint4 x = __ldcg(g4 + j);
-            v[4 * j] = x.x;
-            v[4 * j + 1] = x.y;
-            v[4 * j + 2] = x.z;
-            v[4 * j + 3] = x.w;
-        }
-    }
-    uint32_t sum = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) sum += v[j];
-    uint32_t incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
-        if (lane + o < 32) incl += y;
-    }
-    if (lane == 0) sm->wcnt[warp] = incl;
+    const int gm = static_cast<int>(__ldcg(gh + kGHistBins)) - 1;   // largest bin of any entry
+    if (gm < 0) return 0;
     if (tid == 0) {
         sm->bnd.bin = -1;
         sm->bnd.above = 0u;
     }
-    __syncthreads();
-    uint32_t after = incl - sum, total = 0;
+    // the 256 bins below the largest: thread t holds bin gm - 255 + t
+    {
+        const int bt = gm - (kWinBins - 1) + tid;
+        const uint32_t v = bt >= 0 ? __ldcg(gh + bt) : 0u;
+        uint32_t incl = v;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const uint32_t x = sm->wcnt[q];
-        after += q > warp ? x : 0u;
-        total += x;
-    }
-    const uint32_t kk = min(static_cast<uint32_t>(k), total);
-    if (kk > 0u && after < kk && kk <= after + sum) {
-        uint32_t acc = after;
-#pragma unroll
-        for (int j = 31; j >= 0; --j) {
-            if (acc < kk && kk <= acc + v[j]) {
-                sm->bnd.bin = 32 * tid + j;
-                sm->bnd.above = acc + v[j];   // entries at or above the bin
-            }
-            acc += v[j];
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+            if (lane + o < 32) incl += y;
         }
+        if (lane == 0) sm->wcnt[warp] = incl;
+        __syncthreads();
+        uint32_t after = incl - v;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) after += q > warp ? sm->wcnt[q] : 0u;
+        const uint32_t kk = static_cast<uint32_t>(k);
+        if (after < kk && kk <= after + v) {
+            sm->bnd.bin = bt;
+            sm->bnd.above = after + v;   // entries at or above the bin
+        }
+        __syncthreads();
     }
-    __syncthreads();
+    if (sm->bnd.bin < 0) {
+        // fewer than k entries in those bins: the suffix over all 8192 bins
+        // (thread t holds bins 32 t .. 32 t + 31)
+        uint32_t v[32];
+        {
+            const uint4* g4 = reinterpret_cast<const uint4*>(gh) + 8 * tid;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 x = __ldcg(g4 + j);
+                v[4 * j] = x.x;
+                v[4 * j + 1] = x.y;
+                v[4 * j + 2] = x.z;
+                v[4 * j + 3] = x.w;
+            }
+        }
+        uint32_t sum = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sum += v[j];
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+            if (lane + o < 32) incl += y;
+        }
+        __syncthreads();
+        if (lane == 0) sm->wcnt[warp] = incl;
+        __syncthreads();
+        uint32_t after = incl - sum, total = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint32_t x = sm->wcnt[q];
+            after += q > warp ? x : 0u;
+            total += x;
+        }
+        const uint32_t kk = min(static_cast<uint32_t>(k), total);
+        if (kk > 0u && after < kk && kk <= after + sum) {
+            uint32_t acc = after;
+#pragma unroll
+            for (int j = 31; j >= 0; --j) {
+                if (acc < kk && kk <= acc + v[j]) {
+                    sm->bnd.bin = 32 * tid + j;
+                    sm->bnd.above = acc + v[j];
+                }
+                acc += v[j];
+            }
+        }
+        __syncthreads();
+    }
     const int bstar = sm->bnd.bin;
     const uint32_t ncand = sm->bnd.above;
     if (bstar < 0) return 0;
     uint64_t* cand = buf + 2048;
     if (ncand <= 2048u) {
-        // each run's prefix at or above the boundary bin, per warp into segments
-        // of the candidate buffer (two passes: count, then write at offsets)
-        auto walk = [&](auto f) {
-            for (int j = warp; j < nseg; j += kTopkThreads / 32) {
-                const unsigned long long* rr = reinterpret_cast<const unsigned long long*>(runs) + static_cast<int64_t>(j) * k;
-                for (int m = 0; m < k; m += 32) {
-                    const int e = m + lane;
-                    const uint64_t c = e < k ? static_cast<uint64_t>(__ldcg(rr + e)) : 0ull;
-                    const bool t = c != 0ull && static_cast<int>(win_bin(comp_key(c))) >= bstar;
-                    f(c, t);
-                    if (!__any_sync(0xffffffffu, t)) break;
+        uint32_t* cnt = &sm->red[0];
+        // open runs of a round: two lists of 128 in sm->scratch, used in turn
+        if (tid == 0) {
+            *cnt = 0u;
+            sm->red[2] = 0u;
+            sm->red[3] = 0u;
+        }
+        __syncthreads();
+        const unsigned long long* rr = reinterpret_cast<const unsigned long long*>(runs);
+        auto append = [&](uint64_t c, bool t) {
+            const unsigned bal = __ballot_sync(0xffffffffu, t);
+            uint32_t base = 0u;
+            if (lane == 0 && bal != 0u) base = atomicAdd(cnt, static_cast<uint32_t>(__popc(bal)));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            const uint32_t pos = base + static_cast<uint32_t>(__popc(bal & ((1u << lane) - 1u)));
+            if (t && pos < 2048u) cand[pos] = c;
+        };
+        auto round_len = [&](int open, int m) {
+            int r = ((4 * kTopkThreads / open) + 31) & ~31;
+            r = r < 32 ? 32 : r;
+            return r < k - m ? r : k - m;
+        };
+        // every run is open at first; an open run holds at least R candidates
+        // (R >= 32 or the run's end), so at most 64 stay open after a round
+        int m = 0, nopen = nseg, li = 0;
+        bool all = true;
+        int R = round_len(nseg, 0);
+        while (true) {
+            const int nflat = nopen * R;
+            const uint32_t* cur_list = sm->scratch + 128 * li;
+            uint32_t* next_list = sm->scratch + 128 * (li ^ 1);
+            uint32_t* next_n = &sm->red[2 + (li ^ 1)];
+            for (int f0 = 0; f0 < nflat; f0 += 4 * kTopkThreads) {
+                uint64_t c[4];
+                int jr[4], e[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int f = f0 + q * kTopkThreads + tid;
+                    const int jj = f / R;
+                    e[q] = f - jj * R;
+                    jr[q] = f < nflat ? (all ? jj : static_cast<int>(cur_list[jj])) : 0;
+                    c[q] = f < nflat ? static_cast<uint64_t>(__ldcg(rr + static_cast<int64_t>(jr[q]) * k + m + e[q]))
+                                     : 0ull;
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const bool t = c[q] != 0ull && static_cast<int>(win_bin(comp_key(c[q]))) >= bstar;
+                    append(c[q], t);
+                    if (t && e[q] == R - 1 && m + R < k) next_list[atomicAdd(next_n, 1u) & 127u] = static_cast<uint32_t>(jr[q]);
                 }
             }
-        };
-        const uint32_t got = block_collect(walk, [](uint64_t) { return true; }, cand, 2048u, sm->scratch);
-        const int nout = small_select(cand, static_cast<int>(min(got, 2048u)), k, buf, hist, cur, sm);
-        for (int i = tid; i < nout; i += kTopkThreads) buf[i] = cand[i];
+            __syncthreads();
+            nopen = static_cast<int>(min(*next_n, 128u));
+            if (nopen == 0) break;
+            if (tid == 0) sm->red[2 + li] = 0u;   // the list read this round is written next
+            m += R;
+            li ^= 1;
+            all = false;
+            R = round_len(nopen, m);
+            __syncthreads();
+        }
+        const int got = static_cast<int>(min(*cnt, 2048u));
+        // keys lie in [the boundary bin's floor, the top of the largest bin]
+        const uint32_t lo = static_cast<uint32_t>(bstar) << kWinShift;
+        const uint32_t hi = static_cast<uint32_t>((static_cast<uint64_t>(gm + 1) << kWinShift) - 1u);
+        bin_order(cand, got, buf, lo, hi, hist, cur, sm);
+        for (int i = tid; i < got; i += kTopkThreads) buf[i] = cand[i];
         __syncthreads();
-        return nout;
+        return min(k, got);
     }
     return seg_select(GCompSet{runs, nseg * k}, k, hist, buf, sm);
 }

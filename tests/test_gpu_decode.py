@@ -103,14 +103,25 @@ def test_multisegment_ties(mode, k):
     # chunk is candidates (fp8: more than a CTA's candidate list holds), the
     # refinement runs through the index bits, and for k = 2048 the merge of
     # the tied runs refines as well; the top-k is the first k positions
-    S = 70000 if mode == 0 else 20000
-    W = wl.make_workload("mties", [S, 3000], [1, 1], topk=k, seed=41 + mode)
+    W = wl.make_workload("mties", [70000, 3000], [1, 1], topk=k, seed=41 + mode)
     for b in range(W.batch):
         W.keys[b][:] = W.keys[b][0]
     got = run_decode(W, mode)
     assert np.array_equal(got["idx"][0], np.arange(k))
     assert np.array_equal(got["idx"][1], np.arange(k))
     assert np.all(got["score"][0] == got["score"][0][0])
+
+
+@pytest.mark.parametrize("k", [512, 1024])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_multisegment_random(mode, k):
+    # lengths at and just past a segment (8 chunks of 8192 keys), a 5-segment
+    # sequence and a short one in the same batch: every row against the oracle
+    W = wl.make_workload("mseg", [65536, 65537, 300000, 131073, 777], [1] * 5, topk=k, seed=51 + mode + k)
+    got = run_decode(W, mode)
+    check(W, mode, got)
+    for b in range(W.batch):
+        assert got["idx"][b][0] == W.needle_pos[b]
 
 
 def test_topk_2048_one_and_two_segments():
