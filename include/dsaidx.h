@@ -246,6 +246,22 @@ const char* idx_status_str(idx_status status);
  */
 idx_status idx_test_set_wait_limit(unsigned long long limit_ns);
 
+/*
+ * Per-kernel timing of the score calls (library utility; no passage).
+ * idx_kernel_timing(capacity), capacity > 0: every later score call records
+ * a CUDA event before and after each kernel it launches, on the call's
+ * stream, for up to `capacity` kernels (decode: one kernel per call; prefill:
+ * the scoring kernel, then the row selection); capacity 0 stops and frees
+ * the events.  Returns the capacity set, 0 when stopped, -1 on a CUDA error.
+ * idx_kernel_times(out_ms, max) waits for the recorded events, writes the
+ * durations in milliseconds of up to `max` recorded kernels in launch order
+ * to host array out_ms (nullable: only counts), starts a new record and
+ * returns how many it wrote (-1 on a CUDA error).  Not for calls issued
+ * during stream capture.
+ */
+int idx_kernel_timing(int capacity);
+int idx_kernel_times(float* out_ms, int max);
+
 #ifdef __cplusplus
 }
 #endif

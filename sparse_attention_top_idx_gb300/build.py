@@ -2,7 +2,9 @@
 
 Each .cu under csrc/ is compiled by nvcc in parallel and linked into
 sparse_attention_top_idx_gb300/libdsaidx.so.  No cmake; a rebuild happens only
-when a source or header is newer than the library.
+when a source or header is newer than the library.  build_peak() compiles the
+tensor-core throughput probe (peak/mma_peak.cu) into libmmapeak.so, which the
+benchmark uses as the denominator of the prefill roofline.
 """
 from __future__ import annotations
 
@@ -18,6 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsaidx.so")
+PEAK_SRC = os.path.join(HERE, "peak", "mma_peak.cu")
+PEAK_LIB = os.path.join(HERE, "libmmapeak.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
@@ -78,6 +82,21 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_peak(force: bool = False) -> str:
+    """Compile and link libmmapeak.so (the tcgen05 throughput probe)."""
+    deps = [PEAK_SRC, os.path.join(CSRC, "common.cuh"), os.path.abspath(__file__)]
+    if not force and os.path.exists(PEAK_LIB) and all(os.path.getmtime(d) <= os.path.getmtime(PEAK_LIB) for d in deps):
+        return PEAK_LIB
+    tmp = PEAK_LIB + ".tmp.%d" % os.getpid()
+    cmd = [nvcc()] + ARCH + NVCC_FLAGS + ["-shared", PEAK_SRC, "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (PEAK_SRC, r.stdout, r.stderr))
+    os.replace(tmp, PEAK_LIB)
+    return PEAK_LIB
+
+
 if __name__ == "__main__":
     import sys
     print(build(force="--force" in sys.argv, verbose=True))
+    print(build_peak(force="--force" in sys.argv))

@@ -82,7 +82,10 @@ cudaError_t launch_decode_t(const idx_cache* c, const ScoreParams& p, int64_t un
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, c->tmap, p);
+    kt_mark(st);
+    e = cudaLaunchKernelEx(&cfg, kern, c->tmap, p);
+    kt_mark(st);
+    return e;
 }
 
 }  // namespace

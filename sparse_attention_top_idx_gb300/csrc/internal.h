@@ -179,6 +179,8 @@ cudaError_t launch_store(const idx_cache* c, const void* k, const int64_t* slots
                          int32_t* status, cudaStream_t st);
 cudaError_t launch_decode(const idx_cache* c, const ScoreParams& p, cudaStream_t st);
 cudaError_t launch_prefill(const idx_cache* c, const ScoreParams& p, cudaStream_t st);
+// Per-kernel timing hook (ktimer.cu): records the next event when timing is on.
+void kt_mark(cudaStream_t st);
 
 // Decode geometry for a batch shape: clusters of `cluster` CTAs, chunks of at
 // most `chunk` keys, at most `nseg_max` segments (work units) per sequence.

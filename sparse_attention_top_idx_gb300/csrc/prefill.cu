@@ -81,14 +81,18 @@ cudaError_t launch_prefill_t(const idx_cache* c, const ScoreParams& p, cudaStrea
     cudaError_t e = set_smem_once(kern, plan.total, attr_done);
     if (e != cudaSuccess) return e;
     if (p.num_groups > 0) {
+        kt_mark(st);
         kern<<<p.num_groups, kPrefillThreads, plan.total, st>>>(c->tmap, p);
+        kt_mark(st);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     const SelectPlan sp = select_plan();
     e = set_smem_once(prefill_select_kernel, sp.total, sel_attr_done);
     if (e != cudaSuccess) return e;
+    kt_mark(st);
     prefill_select_kernel<<<p.total_q, kTopkThreads, sp.total, st>>>(p);
+    kt_mark(st);
     return cudaGetLastError();
 }
 

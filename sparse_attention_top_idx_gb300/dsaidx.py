@@ -72,6 +72,10 @@ def load(path: Optional[str] = None):
     L.idx_status_str.restype = ctypes.c_char_p
     L.idx_test_set_wait_limit.argtypes = [ctypes.c_ulonglong]
     L.idx_test_set_wait_limit.restype = I
+    L.idx_kernel_timing.argtypes = [ctypes.c_int]
+    L.idx_kernel_timing.restype = ctypes.c_int
+    L.idx_kernel_times.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    L.idx_kernel_times.restype = ctypes.c_int
     if path is None:
         _lib = L
     return L
@@ -265,3 +269,22 @@ def test_set_wait_limit(limit_ns: int = 0):
     """idx_test_set_wait_limit: shorten the decode kernel's pipeline waits (and
     withhold one MMA signal) so that the timeout path runs; 0 restores."""
     _check(load().idx_test_set_wait_limit(int(limit_ns)), "idx_test_set_wait_limit")
+
+
+def kernel_timing(capacity: int) -> int:
+    """idx_kernel_timing: record CUDA events around each kernel of the next
+    score calls (up to `capacity` kernels); 0 stops."""
+    r = load().idx_kernel_timing(int(capacity))
+    if r < 0:
+        raise RuntimeError("idx_kernel_timing failed")
+    return r
+
+
+def kernel_times(max_kernels: int = 4096):
+    """idx_kernel_times: durations (ms) of the kernels recorded since the last
+    read, in launch order; starts a new record."""
+    buf = (ctypes.c_float * max_kernels)()
+    n = load().idx_kernel_times(ctypes.cast(buf, ctypes.c_void_p), max_kernels)
+    if n < 0:
+        raise RuntimeError("idx_kernel_times failed")
+    return [buf[i] for i in range(n)]

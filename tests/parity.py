@@ -20,22 +20,9 @@ import torch
 
 from sparse_attention_top_idx_gb300 import dsaidx
 from sparse_attention_top_idx_gb300 import workloads as wl
+from sparse_attention_top_idx_gb300.host import bf16_tensor, build_cache  # noqa: F401 (re-exported)
 
 TOL = 1e-3
-
-
-def bf16_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(bits, np.uint16).view(np.int16)).view(
-        torch.bfloat16).to(device)
-
-
-def build_cache(W: wl.Workload, mode: int, fill: int = 0xA5, device="cuda"):
-    cache = dsaidx.IndexCache.allocate(W.num_blocks, W.bs, mode, device=device, fill=fill)
-    if sum(W.seq_lens):
-        k = bf16_tensor(W.all_keys(), device)
-        slots = torch.from_numpy(W.all_slots()).to(device)
-        dsaidx.store_keys(cache, k, slots)
-    return cache
 
 
 def decode_inputs(W: wl.Workload, device="cuda"):

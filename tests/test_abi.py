@@ -16,7 +16,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = dsaidx.header_functions()
-    assert len(names) == 13, names
+    assert len(names) == 15, names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -52,5 +52,7 @@ def test_host_argument_checks(lib):
     v = ctypes.c_int32()
     assert lib.idx_read_device_status(None, None, ctypes.byref(v)) == 1
     assert lib.idx_test_set_wait_limit(0) == 0     # restores the normal limit
+    assert lib.idx_kernel_timing(0) == 0            # timing off: no events
+    assert lib.idx_kernel_times(None, 0) == 0
     assert dsaidx.status_str(0) == "ok"
     assert dsaidx.status_str(4) == "workspace too small"

@@ -88,3 +88,20 @@ def test_bad_block_id_flags_rows():
     assert np.all(got["idx"][:5] == -1)
     ref, nvis = oracle_ref(W, dsaidx.FP8, range(5, 11))
     check_rows(got, ref, nvis, 64, rows=range(5, 11))
+
+
+def test_kernel_timing_records_each_kernel():
+    # prefill launches the scoring kernel and the row select; decode one kernel
+    W = wl.make_workload("ktime", [700, 300], [5, 3], topk=64, seed=91)
+    cache = build_cache(W, dsaidx.FP8)
+    dsaidx.kernel_timing(16)
+    run_prefill(W, dsaidx.FP8, cache=cache)
+    t = dsaidx.kernel_times()
+    assert len(t) == 2 and all(x > 0.0 for x in t)
+    D = wl.make_workload("ktime_dec", [700, 300], [1, 1], topk=64, seed=92)
+    run_decode(D, dsaidx.FP8)
+    t = dsaidx.kernel_times()
+    assert len(t) == 1 and t[0] > 0.0
+    dsaidx.kernel_timing(0)
+    run_decode(D, dsaidx.FP8)
+    assert dsaidx.kernel_times() == []
