@@ -83,6 +83,11 @@ class Oracle:
         L.orc_block_bytes.restype = I64
         L.orc_store_keys.argtypes = [P, I64, I, I, I, P, P, I64]
         L.orc_store_keys.restype = I64
+        L.orc_store_keys_any.argtypes = [P, I64, I, I, I, P, P, I64, I]
+        L.orc_store_keys_any.restype = I64
+        L.orc_wht_rows.argtypes = [P, I64, I, P]
+        L.orc_quant_rows_f32.argtypes = [P, I64, I, P, P]
+        L.orc_f32_to_bf16_n.argtypes = [P, P, I64]
         L.orc_gather_keys.argtypes = [P, I, I, I, P, I64, P, P, P]
         L.orc_scores_row.argtypes = [I, I, I, P, P, I64, P, P, P, P, P]
         L.orc_topk_row.argtypes = [P, I64, I, P, P]
@@ -136,6 +141,43 @@ class Oracle:
         return codes, scales
 
 
+    def quantize_rows_f32(self, x):
+        """Per-row fp8 quantisation of float rows [R, d] -> (codes [R, d], scales [R])."""
+        x = _c(x, np.float32)
+        R, d = x.shape
+        codes = np.empty((R, d), np.uint8)
+        scales = np.empty(R, np.float32)
+        self.L.orc_quant_rows_f32(_p(x), R, d, _p(codes), _p(scales))
+        return codes, scales
+
+
+    def wht_rows(self, x_bf16) -> np.ndarray:
+        """Walsh-Hadamard rotation of bf16 rows [R, d] (d a power of two):
+        float rows y = H x, H orthonormal in Sylvester order."""
+        x = _c(x_bf16, np.uint16)
+        R, d = x.shape
+        y = np.empty((R, d), np.float32)
+        self.L.orc_wht_rows(_p(x), R, d, _p(y))
+        return y
+
+
+    def rotated_key_rows(self, x_bf16, dtype: int):
+        """What the rotated store keeps for bf16 key rows: fp8 (codes, scales)
+        of the rotated floats, or their bf16 bits rounded to nearest even."""
+        y = self.wht_rows(x_bf16)
+        if dtype == FP8:
+            return self.quantize_rows_f32(y)
+        return self.f32_to_bf16(y)
+
+
+    def f32_to_bf16(self, x) -> np.ndarray:
+        """float -> bf16 bits, round to nearest even (finite values)."""
+        x = _c(x, np.float32)
+        out = np.empty(x.shape, np.uint16)
+        self.L.orc_f32_to_bf16_n(_p(x), _p(out), x.size)
+        return out
+
+
     # --------------------------------------------------------------------------
     # paged cache
     # --------------------------------------------------------------------------
@@ -144,15 +186,17 @@ class Oracle:
         return int(self.L.orc_block_bytes(dtype, bs, d))
 
 
-    def store_keys(self, pool: np.ndarray, k_bf16, slot_mapping, bs: int, dtype: int) -> int:
-        """Write keys into a flat uint8 pool in place; returns tokens written."""
+    def store_keys(self, pool: np.ndarray, k_bf16, slot_mapping, bs: int, dtype: int,
+                   rotate: bool = False) -> int:
+        """Write keys into a flat uint8 pool in place (Walsh-Hadamard rotated
+        first when rotate); returns tokens written."""
         assert pool.dtype == np.uint8 and pool.flags.c_contiguous
         k = _c(k_bf16, np.uint16)
         sm = _c(slot_mapping, np.int64)
         n, d = k.shape
         bb = self.block_bytes(dtype, bs, d)
         nb = pool.size // bb
-        r = self.L.orc_store_keys(_p(pool), nb, bs, d, dtype, _p(k), _p(sm), n)
+        r = self.L.orc_store_keys_any(_p(pool), nb, bs, d, dtype, _p(k), _p(sm), n, 1 if rotate else 0)
         if r < 0:
             raise ValueError("slot out of range")
         return int(r)

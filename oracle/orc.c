@@ -52,6 +52,9 @@
 /* ------------------------------------------------------------------------ */
 
 /* A bf16 value is the top half of an fp32 bit pattern. */
+/* Largest row length the per-row helpers take (the index keys have d = 128). */
+#define ORC_MAX_D 1024
+
 float orc_bf16_to_f32(uint16_t b)
 {
     uint32_t u = ((uint32_t)b) << 16;
@@ -154,15 +157,16 @@ void orc_e4m3_decode_n(const uint8_t* c, float* out, int64_t n)
 }
 
 /*
- * Per-row fp8 quantisation: amax over the row, scale = fl32(amax / 448),
- * code_i = e4m3(fl32(x_i / scale)).  A zero row gets scale 0 and zero codes.
+ * Per-row fp8 quantisation of d float values: amax over the row, scale =
+ * fl32(amax / 448), code_i = e4m3(fl32(x_i / scale)).  A zero row gets scale
+ * 0 and zero codes.
  */
-void orc_quant_row(const uint16_t* x_bf16, int d, uint8_t* codes, float* scale_out)
+void orc_quant_row_f32(const float* x, int d, uint8_t* codes, float* scale_out)
 {
     float amax = 0.0f, scale;
     int i;
     for (i = 0; i < d; i++) {
-        float v = fabsf(orc_bf16_to_f32(x_bf16[i]));
+        float v = fabsf(x[i]);
         if (v > amax)
             amax = v;
     }
@@ -172,10 +176,92 @@ void orc_quant_row(const uint16_t* x_bf16, int d, uint8_t* codes, float* scale_o
         if (amax == 0.0f) {
             codes[i] = 0x00;
         } else {
-            float y = orc_bf16_to_f32(x_bf16[i]) / scale;
+            float y = x[i] / scale;
             codes[i] = orc_e4m3_encode(y);
         }
     }
+}
+
+/* The same for a row of bf16 values (each exactly a float). */
+void orc_quant_row(const uint16_t* x_bf16, int d, uint8_t* codes, float* scale_out)
+{
+    float x[ORC_MAX_D];
+    int i;
+    for (i = 0; i < d && i < ORC_MAX_D; i++)
+        x[i] = orc_bf16_to_f32(x_bf16[i]);
+    orc_quant_row_f32(x, d < ORC_MAX_D ? d : ORC_MAX_D, codes, scale_out);
+}
+
+void orc_quant_rows_f32(const float* x, int64_t rows, int d, uint8_t* codes, float* scales)
+{
+    int64_t r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; r++)
+        orc_quant_row_f32(x + r * d, d, codes + r * d, scales + r);
+}
+
+/* float -> bf16 bits, round to nearest even (finite inputs). */
+uint16_t orc_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    u = u + 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+void orc_f32_to_bf16_n(const float* x, uint16_t* out, int64_t n)
+{
+    int64_t i;
+    for (i = 0; i < n; i++)
+        out[i] = orc_f32_to_bf16(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Walsh-Hadamard rotation of an index key                                   */
+/* ------------------------------------------------------------------------ */
+
+/* 1 when v has an odd number of set bits. */
+static int orc_odd_parity(unsigned v)
+{
+    int p = 0;
+    while (v) {
+        p ^= (int)(v & 1u);
+        v >>= 1;
+    }
+    return p;
+}
+
+/*
+ * y = H x for one row of d bf16 values (d a power of two), H the orthonormal
+ * Walsh-Hadamard matrix in Sylvester order, H[i][j] = (-1)^popcount(i & j) /
+ * sqrt(d): the rotation that "DeepSeek-V4 index_topk=1024 sparse indexer
+ * can't recall verbatim lines" (ROCm/ATOM issue #1507), section "Root cause",
+ * says the index query gets and the index key must get too (its fix (B) puts
+ * it on the key store path); H is orthogonal, so (Hq).(Hk) = q.k.  The +-1
+ * sum is taken in double (exact for a row whose exponents span at most 38
+ * binades), multiplied by the double nearest 1/sqrt(d) and rounded once to
+ * float.
+ */
+void orc_wht_row(const uint16_t* x_bf16, int d, float* y)
+{
+    const double c = 1.0 / sqrt((double)d);
+    int i, j;
+    for (i = 0; i < d; i++) {
+        double s = 0.0;
+        for (j = 0; j < d; j++) {
+            double v = (double)orc_bf16_to_f32(x_bf16[j]);
+            s += orc_odd_parity((unsigned)(i & j)) ? -v : v;
+        }
+        y[i] = (float)(s * c);
+    }
+}
+
+void orc_wht_rows(const uint16_t* x_bf16, int64_t rows, int d, float* y)
+{
+    int64_t r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; r++)
+        orc_wht_row(x_bf16 + r * d, d, y + r * d);
 }
 
 void orc_quant_rows(const uint16_t* x_bf16, int64_t rows, int d, uint8_t* codes, float* scales)
@@ -207,14 +293,20 @@ int64_t orc_block_bytes(int dtype, int bs, int d)
 
 /*
  * Write n keys into the pool: token i goes to slot slot_mapping[i] =
- * block * bs + offset; a negative slot is skipped.  Returns the number of
- * tokens written, or -1 if a slot is out of range.
+ * block * bs + offset; a negative slot is skipped.  With rotate != 0 each key
+ * is first Walsh-Hadamard rotated (orc_wht_row) and the float result is what
+ * is quantised (fp8) or rounded to bf16.  Returns the number of tokens
+ * written, or -1 if a slot is out of range (-2 for d > ORC_MAX_D).
  */
-int64_t orc_store_keys(uint8_t* pool, int64_t num_blocks, int bs, int d, int dtype,
-                       const uint16_t* k_bf16, const int64_t* slot_mapping, int64_t n)
+int64_t orc_store_keys_any(uint8_t* pool, int64_t num_blocks, int bs, int d, int dtype,
+                           const uint16_t* k_bf16, const int64_t* slot_mapping, int64_t n, int rotate)
 {
     int64_t i, written = 0;
     int64_t bb = orc_block_bytes(dtype, bs, d);
+    float y[ORC_MAX_D];
+    int j;
+    if (d > ORC_MAX_D)
+        return -2;
     for (i = 0; i < n; i++) {
         int64_t slot = slot_mapping[i];
         int64_t blk, off;
@@ -226,16 +318,32 @@ int64_t orc_store_keys(uint8_t* pool, int64_t num_blocks, int bs, int d, int dty
         if (blk >= num_blocks)
             return -1;
         base = pool + blk * bb;
+        if (rotate)
+            orc_wht_row(k_bf16 + i * d, d, y);
         if (dtype == ORC_FP8) {
             float sc;
-            orc_quant_row(k_bf16 + i * d, d, base + off * d, &sc);
+            if (rotate)
+                orc_quant_row_f32(y, d, base + off * d, &sc);
+            else
+                orc_quant_row(k_bf16 + i * d, d, base + off * d, &sc);
             memcpy(base + (int64_t)bs * d + off * 4, &sc, 4);
+        } else if (rotate) {
+            for (j = 0; j < d; j++) {
+                uint16_t b = orc_f32_to_bf16(y[j]);
+                memcpy(base + off * d * 2 + (int64_t)j * 2, &b, 2);
+            }
         } else {
             memcpy(base + off * d * 2, k_bf16 + i * d, (size_t)d * 2);
         }
         written++;
     }
     return written;
+}
+
+int64_t orc_store_keys(uint8_t* pool, int64_t num_blocks, int bs, int d, int dtype,
+                       const uint16_t* k_bf16, const int64_t* slot_mapping, int64_t n)
+{
+    return orc_store_keys_any(pool, num_blocks, bs, d, dtype, k_bf16, slot_mapping, n, 0);
 }
 
 /*

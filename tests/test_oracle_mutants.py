@@ -33,6 +33,12 @@ MUTANTS = {
     "scale_slot_stride": ("memcpy(base + (int64_t)bs * d + off * 4, &sc, 4);",
                           "memcpy(base + (int64_t)bs * d + off, &sc, 4);"),
     "subnormal_step": ("q = ldexp(1.0, -9);", "q = ldexp(1.0, -8);"),
+    "wht_sign": ("s += orc_odd_parity((unsigned)(i & j)) ? -v : v;",
+                 "s += orc_odd_parity((unsigned)(i & j)) ? v : -v;"),
+    "wht_no_normalisation": ("const double c = 1.0 / sqrt((double)d);", "const double c = 1.0;"),
+    "wht_index_or": ("s += orc_odd_parity((unsigned)(i & j)) ? -v : v;",
+                     "s += orc_odd_parity((unsigned)(i | j)) ? -v : v;"),
+    "bf16_round_half_up": ("u = u + 0x7FFFu + ((u >> 16) & 1u);", "u = u + 0x8000u;"),
 }
 
 
@@ -88,6 +94,19 @@ def battery(O) -> bool:
             return False
         if p + 1 <= 8 and set(sel.tolist()) != set(range(p + 1)):
             return False
+    # Walsh-Hadamard rotation: the Kronecker-built Sylvester matrix over sqrt(d)
+    E = np.zeros((128, 128), np.uint16)
+    E[np.arange(128), np.arange(128)] = 0x3F80
+    S = np.ones((1, 1))
+    while S.shape[0] < 128:
+        S = np.kron(np.array([[1.0, 1.0], [1.0, -1.0]]), S)
+    if not np.array_equal(O.wht_rows(E), (S / np.sqrt(128.0)).astype(np.float32)):
+        return False
+    # float -> bf16 rounding against numpy, ties included
+    xt = np.concatenate([rng.standard_normal(5000).astype(np.float32),
+                         (np.arange(1, 500, dtype=np.uint32) << 16 | 0x8000).view(np.float32)])
+    if not np.array_equal(O.f32_to_bf16(xt), wl.f32_to_bf16_bits(xt)):
+        return False
     # store round trip at bs 64
     Wk = wl.make_workload("st", [100], [1], bs=64, seed=4)
     pool = np.zeros(Wk.num_blocks * 8448, np.uint8)
