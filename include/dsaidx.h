@@ -128,6 +128,24 @@ idx_status idx_store_keys(const idx_cache* cache, const void* k_bf16_dev,
                           int32_t* status_dev, void* stream);
 
 /*
+ * idx_store_keys with each key first Walsh-Hadamard rotated: the fix (B) of
+ * "DeepSeek-V4 index_topk=1024 sparse indexer can't recall verbatim lines"
+ * (ROCm/ATOM issue #1507, section "Root cause"), which rotates the index key
+ * on the store path to match the rotated index query, so that scores use
+ * (Hq).(Hk) = q.k.  H is the orthonormal 128-point Walsh-Hadamard matrix in
+ * Sylvester order, H[i][j] = (-1)^popcount(i & j) / sqrt(128).  The +-1 sums
+ * of the bf16 inputs are formed exactly in double (exact for rows whose
+ * exponents span at most 38 binades), multiplied by the double nearest
+ * 1/sqrt(128) and rounded once to float; that float row is quantised as
+ * above (fp8) or rounded to bf16, nearest even (bf16 pools).  Same
+ * arguments, layout, ownership and errors as idx_store_keys.  The caller
+ * supplies queries already rotated (the score calls do not rotate).
+ */
+idx_status idx_store_keys_rotated(const idx_cache* cache, const void* k_bf16_dev,
+                                  const int64_t* slot_mapping_dev, int64_t n,
+                                  int32_t* status_dev, void* stream);
+
+/*
  * Workspace bytes a decode call needs for this batch shape (depends on the
  * handle's device and key format).  0 on invalid arguments.
  */
@@ -167,6 +185,25 @@ idx_status idx_score_topk_decode(const idx_cache* cache, const void* q_bf16_dev,
                                  int batch, int max_seq_len, int heads, int topk,
                                  int32_t* out_idx_dev, float* out_score_dev,
                                  void* workspace_dev, size_t ws_bytes, void* stream);
+
+/*
+ * idx_score_topk_decode that also writes each selected key's physical pool
+ * slot: out_slot_dev (nullable, [batch, topk] int64, 8-byte aligned) gets
+ * block_table[b][s / block_size] * block_size + s % block_size for selected
+ * logical index s and -1 where out_idx is -1 -- the logical-to-physical
+ * translate (csa_translate_pack) that "DeepSeek-V4 index_topk=1024 sparse
+ * indexer can't recall verbatim lines" (ROCm/ATOM issue #1507, section "How it
+ * was isolated") runs on the selected indices before sparse attention.  An
+ * index whose block lies past max_blocks_per_seq gets -1.  Otherwise the same
+ * arguments, results and errors as idx_score_topk_decode.
+ */
+idx_status idx_score_topk_decode_slots(const idx_cache* cache, const void* q_bf16_dev,
+                                       const float* w_dev, const int32_t* block_table_dev,
+                                       int max_blocks_per_seq, const int32_t* seq_lens_dev,
+                                       int batch, int max_seq_len, int heads, int topk,
+                                       int32_t* out_idx_dev, float* out_score_dev,
+                                       int64_t* out_slot_dev, void* workspace_dev, size_t ws_bytes,
+                                       void* stream);
 
 /*
  * Decode without a workspace argument, for callers that cannot allocate
@@ -222,6 +259,20 @@ idx_status idx_score_topk_prefill(const idx_cache* cache, const void* q_bf16_dev
                                   int max_seq_len, int heads, int topk,
                                   int32_t* out_idx_dev, float* out_score_dev,
                                   void* workspace_dev, size_t ws_bytes, void* stream);
+
+/*
+ * idx_score_topk_prefill that also writes each selected key's physical pool
+ * slot to out_slot_dev (nullable, [total_q, topk] int64, 8-byte aligned; -1
+ * where out_idx is -1), the translate described at
+ * idx_score_topk_decode_slots.  Otherwise the same as idx_score_topk_prefill.
+ */
+idx_status idx_score_topk_prefill_slots(const idx_cache* cache, const void* q_bf16_dev,
+                                        const float* w_dev, const int32_t* cu_seqlens_q_dev,
+                                        const int32_t* seq_lens_dev, const int32_t* block_table_dev,
+                                        int max_blocks_per_seq, int batch, int total_q, int max_seq_len,
+                                        int heads, int topk, int32_t* out_idx_dev, float* out_score_dev,
+                                        int64_t* out_slot_dev, void* workspace_dev, size_t ws_bytes,
+                                        void* stream);
 
 /*
  * Synchronise `stream` and read the device status word of a workspace into

@@ -88,6 +88,7 @@ class Oracle:
         L.orc_wht_rows.argtypes = [P, I64, I, P]
         L.orc_quant_rows_f32.argtypes = [P, I64, I, P, P]
         L.orc_f32_to_bf16_n.argtypes = [P, P, I64]
+        L.orc_translate_slots.argtypes = [P, I64, I, P, I64, P]
         L.orc_gather_keys.argtypes = [P, I, I, I, P, I64, P, P, P]
         L.orc_scores_row.argtypes = [I, I, I, P, P, I64, P, P, P, P, P]
         L.orc_topk_row.argtypes = [P, I64, I, P, P]
@@ -200,6 +201,16 @@ class Oracle:
         if r < 0:
             raise ValueError("slot out of range")
         return int(r)
+
+
+    def translate_slots(self, table_row, bs: int, idx) -> np.ndarray:
+        """Physical pool slots of a sequence's selected logical indices (-1 for
+        -1 or a block past the table row)."""
+        t = _c(table_row, np.int32)
+        i = _c(idx, np.int32)
+        out = np.empty(i.shape, np.int64)
+        self.L.orc_translate_slots(_p(t), t.size, bs, _p(i), i.size, _p(out))
+        return out
 
 
     def gather_keys(self, pool: np.ndarray, table_row, S: int, bs: int, dtype: int, d: int = 128):

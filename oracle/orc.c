@@ -347,6 +347,27 @@ int64_t orc_store_keys(uint8_t* pool, int64_t num_blocks, int bs, int d, int dty
 }
 
 /*
+ * Logical-to-physical translate of selected key indices (csa_translate_pack
+ * in "DeepSeek-V4 index_topk=1024 sparse indexer can't recall verbatim
+ * lines", ROCm/ATOM issue #1507, section "How it was isolated"): index s of a
+ * sequence whose block-table row has mbps entries becomes the pool slot
+ * table_row[s / bs] * bs + s % bs; a negative index or a block past the row
+ * becomes -1.
+ */
+void orc_translate_slots(const int32_t* table_row, int64_t mbps, int bs, const int32_t* idx, int64_t n,
+                         int64_t* out)
+{
+    int64_t i;
+    for (i = 0; i < n; i++) {
+        int64_t s = idx[i];
+        if (s < 0 || s / bs >= mbps)
+            out[i] = -1;
+        else
+            out[i] = (int64_t)table_row[s / bs] * bs + s % bs;
+    }
+}
+
+/*
  * Read logical key s of a sequence back out of the pool through its block
  * table row (block = table[s / bs], offset = s % bs).  fp8: codes + scale.
  * bf16: the d raw values.

@@ -152,16 +152,28 @@ idx_status idx_cache_create(idx_cache** out, void* pool_dev, int64_t num_blocks,
 
 void idx_cache_destroy(idx_cache* cache) { delete cache; }
 
-idx_status idx_store_keys(const idx_cache* cache, const void* k_bf16_dev, const int64_t* slot_mapping_dev,
-                          int64_t n, int32_t* status_dev, void* stream) {
+namespace {
+idx_status store_keys_common(const idx_cache* cache, const void* k_bf16_dev, const int64_t* slot_mapping_dev,
+                             int64_t n, int32_t* status_dev, bool rotate, void* stream) {
     if (!cache || n < 0) return IDX_ERR_INVALID_ARG;
     if (n == 0) return IDX_OK;
     if (!k_bf16_dev || !slot_mapping_dev || !aligned(k_bf16_dev, 16) || !aligned(slot_mapping_dev, 8))
         return IDX_ERR_INVALID_ARG;
     if (!same_device(cache)) return IDX_ERR_INVALID_ARG;
-    cudaError_t e = dsaidx::launch_store(cache, k_bf16_dev, slot_mapping_dev, n, status_dev,
+    cudaError_t e = dsaidx::launch_store(cache, k_bf16_dev, slot_mapping_dev, n, status_dev, rotate,
                                          static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+}  // namespace
+
+idx_status idx_store_keys(const idx_cache* cache, const void* k_bf16_dev, const int64_t* slot_mapping_dev,
+                          int64_t n, int32_t* status_dev, void* stream) {
+    return store_keys_common(cache, k_bf16_dev, slot_mapping_dev, n, status_dev, false, stream);
+}
+
+idx_status idx_store_keys_rotated(const idx_cache* cache, const void* k_bf16_dev, const int64_t* slot_mapping_dev,
+                                  int64_t n, int32_t* status_dev, void* stream) {
+    return store_keys_common(cache, k_bf16_dev, slot_mapping_dev, n, status_dev, true, stream);
 }
 
 size_t idx_workspace_bytes_decode(const idx_cache* cache, int batch, int max_seq_len, int heads, int topk) {
@@ -182,7 +194,18 @@ idx_status idx_score_topk_decode(const idx_cache* cache, const void* q_bf16_dev,
                                  const int32_t* seq_lens_dev, int batch, int max_seq_len, int heads,
                                  int topk, int32_t* out_idx_dev, float* out_score_dev, void* workspace_dev,
                                  size_t ws_bytes, void* stream) {
+    return idx_score_topk_decode_slots(cache, q_bf16_dev, w_dev, block_table_dev, max_blocks_per_seq,
+                                       seq_lens_dev, batch, max_seq_len, heads, topk, out_idx_dev, out_score_dev,
+                                       nullptr, workspace_dev, ws_bytes, stream);
+}
+
+idx_status idx_score_topk_decode_slots(const idx_cache* cache, const void* q_bf16_dev, const float* w_dev,
+                                       const int32_t* block_table_dev, int max_blocks_per_seq,
+                                       const int32_t* seq_lens_dev, int batch, int max_seq_len, int heads,
+                                       int topk, int32_t* out_idx_dev, float* out_score_dev,
+                                       int64_t* out_slot_dev, void* workspace_dev, size_t ws_bytes, void* stream) {
     if (!cache) return IDX_ERR_INVALID_ARG;
+    if (out_slot_dev && !aligned(out_slot_dev, 8)) return IDX_ERR_INVALID_ARG;
     if (heads != dsaidx::kHeads) return IDX_ERR_UNSUPPORTED;
     if (batch < 0 || max_seq_len < 0 || topk < 1 || topk > IDX_MAX_TOPK || max_blocks_per_seq < 1)
         return IDX_ERR_INVALID_ARG;
@@ -213,6 +236,8 @@ idx_status idx_score_topk_decode(const idx_cache* cache, const void* q_bf16_dev,
     p.nseg_max = ws.geom.nseg_max;
     p.out_idx = out_idx_dev;
     p.out_score = out_score_dev;
+    p.out_slot = out_slot_dev;
+    p.block_size = cache->block_size;
     p.status = reinterpret_cast<int32_t*>(base);
     p.ctr = reinterpret_cast<uint32_t*>(base + ws.ctr);
     p.seqflag = reinterpret_cast<uint32_t*>(base + ws.seqflag);
@@ -239,7 +264,19 @@ idx_status idx_score_topk_prefill(const idx_cache* cache, const void* q_bf16_dev
                                   const int32_t* block_table_dev, int max_blocks_per_seq, int batch,
                                   int total_q, int max_seq_len, int heads, int topk, int32_t* out_idx_dev,
                                   float* out_score_dev, void* workspace_dev, size_t ws_bytes, void* stream) {
+    return idx_score_topk_prefill_slots(cache, q_bf16_dev, w_dev, cu_seqlens_q_dev, seq_lens_dev, block_table_dev,
+                                        max_blocks_per_seq, batch, total_q, max_seq_len, heads, topk, out_idx_dev,
+                                        out_score_dev, nullptr, workspace_dev, ws_bytes, stream);
+}
+
+idx_status idx_score_topk_prefill_slots(const idx_cache* cache, const void* q_bf16_dev, const float* w_dev,
+                                        const int32_t* cu_seqlens_q_dev, const int32_t* seq_lens_dev,
+                                        const int32_t* block_table_dev, int max_blocks_per_seq, int batch,
+                                        int total_q, int max_seq_len, int heads, int topk, int32_t* out_idx_dev,
+                                        float* out_score_dev, int64_t* out_slot_dev, void* workspace_dev,
+                                        size_t ws_bytes, void* stream) {
     if (!cache) return IDX_ERR_INVALID_ARG;
+    if (out_slot_dev && !aligned(out_slot_dev, 8)) return IDX_ERR_INVALID_ARG;
     if (heads != dsaidx::kHeads) return IDX_ERR_UNSUPPORTED;
     if (batch < 0 || batch > 4096 || total_q < 0 || max_seq_len < 0 || topk < 1 || topk > IDX_MAX_TOPK ||
         max_blocks_per_seq < 1)
@@ -274,6 +311,8 @@ idx_status idx_score_topk_prefill(const idx_cache* cache, const void* q_bf16_dev
     p.num_groups = (total_q + dsaidx::kPrefillQT - 1) / dsaidx::kPrefillQT + batch;
     p.out_idx = out_idx_dev;
     p.out_score = out_score_dev;
+    p.out_slot = out_slot_dev;
+    p.block_size = cache->block_size;
     p.status = reinterpret_cast<int32_t*>(base);
     p.rowflag = reinterpret_cast<uint32_t*>(base + ws.rowflag);
     p.scores = reinterpret_cast<float*>(base + ws.scores);

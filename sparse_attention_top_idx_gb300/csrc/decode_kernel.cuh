@@ -631,12 +631,15 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
             const bool single = nseg == 1;
             int32_t* oi = p.out_idx + static_cast<int64_t>(b) * k;
             float* os = p.out_score ? p.out_score + static_cast<int64_t>(b) * k : nullptr;
+            int64_t* osl = p.out_slot ? p.out_slot + static_cast<int64_t>(b) * k : nullptr;
+            const int32_t* btr = p.block_table + static_cast<int64_t>(b) * p.mbps;
             uint64_t* run_out = single ? nullptr : p.cand + static_cast<int64_t>(b) * p.cand_cap + static_cast<int64_t>(seg) * k;
             uint32_t* gh = single ? nullptr : p.ghist + static_cast<int64_t>(b) * kGHistWords;
             auto emit = [&](int r, uint64_t c) {
                 if (single) {
                     oi[r] = comp_index(c);
                     if (os) os[r] = key_score(comp_key(c));
+                    if (osl) osl[r] = slot_of(btr, p.mbps, kBs, comp_index(c));
                 } else {
                     run_out[r] = c;
                     const uint32_t wb = win_bin(comp_key(c));
@@ -739,6 +742,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                     for (int j = (flag ? 0 : nsel) + tid; j < k; j += kThreads) {
                         oi[j] = -1;
                         if (os) os[j] = -INFINITY;
+                        if (osl) osl[j] = -1;
                     }
                 }
             } else {
@@ -772,7 +776,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                         if (!bad)
                             mout = merge_runs(p.cand + static_cast<int64_t>(b) * p.cand_cap, nseg, k, gh, shist,
                                               reinterpret_cast<uint32_t*>(pool), sbuf, &ks->sel);
-                        write_topk_row(sbuf, mout, k, oi, os);
+                        write_topk_row(sbuf, mout, k, oi, os, osl, btr, p.mbps, kBs);
                         // leave the sequence's workspace zeroed for the next call
                         for (int i = tid; i < kGHistWords; i += kThreads) gh[i] = 0u;
                         if (tid == 0) {
@@ -786,7 +790,8 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
             // an empty sequence, or one whose length is out of range: a -1 row
             if (!valid && tid == 0) set_status(status, IDX_ERR_DEVICE_CHECK);
             write_topk_row(sbuf, -1, p.topk, p.out_idx + static_cast<int64_t>(b) * p.topk,
-                           p.out_score ? p.out_score + static_cast<int64_t>(b) * p.topk : nullptr);
+                           p.out_score ? p.out_score + static_cast<int64_t>(b) * p.topk : nullptr,
+                           p.out_slot ? p.out_slot + static_cast<int64_t>(b) * p.topk : nullptr);
         }
         // generic accesses of the stages come before the next unit's copies
         // into them; this CTA is done with its receive areas

@@ -51,6 +51,8 @@ struct ScoreParams {
     int num_groups;              // prefill: grid bound on query groups
     int32_t* out_idx;
     float* out_score;
+    int64_t* out_slot;           // nullable: physical slot of each selected key (-1 pads)
+    int block_size;              // tokens per pool block (the slot translation)
     // workspace
     int32_t* status;
     uint32_t* ctr;               // decode: [batch] completed-segment tickets
@@ -176,7 +178,7 @@ inline cudaError_t set_smem_once(Kern kern, int bytes, std::atomic<unsigned long
 
 // Kernel launchers (one per translation unit).
 cudaError_t launch_store(const idx_cache* c, const void* k, const int64_t* slots, int64_t n,
-                         int32_t* status, cudaStream_t st);
+                         int32_t* status, bool rotate, cudaStream_t st);
 cudaError_t launch_decode(const idx_cache* c, const ScoreParams& p, cudaStream_t st);
 cudaError_t launch_prefill(const idx_cache* c, const ScoreParams& p, cudaStream_t st);
 // Per-kernel timing hook (ktimer.cu): records the next event when timing is on.

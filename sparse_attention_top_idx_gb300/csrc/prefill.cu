@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kTopkThreads, 3) prefill_select_kernel(const S
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + sp.hist_off);
     uint64_t* sel = reinterpret_cast<uint64_t*>(smem + sp.sel_off);
     SelectSmem* ss = reinterpret_cast<SelectSmem*>(smem + sp.ss_off);
-    __shared__ int s_nvis, s_bad;
+    __shared__ int s_nvis, s_bad, s_b;
     const int r = blockIdx.x;
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -50,15 +50,18 @@ __global__ void __launch_bounds__(kTopkThreads, 3) prefill_select_kernel(const S
         if (flagged) p.rowflag[r] = 0;
         s_bad = flagged || invalid;
         s_nvis = pos + 1;
+        s_b = b;
     }
     for (int i = tid; i < kHistBins; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
     int32_t* oi = p.out_idx + static_cast<int64_t>(r) * p.topk;
     float* os = p.out_score ? p.out_score + static_cast<int64_t>(r) * p.topk : nullptr;
+    int64_t* osl = p.out_slot ? p.out_slot + static_cast<int64_t>(r) * p.topk : nullptr;
     if (s_bad) {
         for (int j = tid; j < p.topk; j += kTopkThreads) {
             oi[j] = -1;
             if (os) os[j] = -INFINITY;
+            if (osl) osl[j] = -1;
         }
         return;
     }
@@ -69,7 +72,8 @@ __global__ void __launch_bounds__(kTopkThreads, 3) prefill_select_kernel(const S
     __syncthreads();
     auto each_slow = [&](auto f) { walk_row_slow(row, nvis, f); };
     const int nout = block_topk_sorted(each, each_slow, hist, p.topk, sel, IDX_MAX_TOPK + kSelBcap, ss);
-    write_topk_row(sel, nout, p.topk, oi, os);
+    write_topk_row(sel, nout, p.topk, oi, os, osl, p.block_table + static_cast<int64_t>(s_b) * p.mbps, p.mbps,
+                   p.block_size);
 }
 
 template <bool kFp8, int kBs>

@@ -12,6 +12,19 @@
 // even, saturating), pairs of lanes merge their 8 code bytes so that 8 lanes
 // write the 128-byte code row as 16-byte stores, and lane 0 writes the scale.
 // bf16: each lane copies its 16 bytes to the slot.
+//
+// Rotated store (idx_store_keys_rotated): the key is first turned by the
+// orthonormal 128-point Walsh-Hadamard transform (Sylvester order), the
+// rotation that "DeepSeek-V4 index_topk=1024 sparse indexer can't recall
+// verbatim lines" (section "Root cause", fix (B)) puts on the key store path
+// to match the rotated index query.  The fast transform's butterflies run in
+// double -- index bits 0..2 inside a lane's 8 values, bits 3..6 across the
+// half-warp by shuffles -- where the +-1 sums of bf16 inputs are exact (row
+// exponents within 38 binades), then one multiply by the double nearest
+// 1/sqrt(128) and one rounding to float; the float row is quantised (fp8) or
+// rounded to bf16 (nearest even).
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,12 +40,44 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float a, float b) {
     return r;
 }
 
-template <bool kFp8>
+// In-place Walsh-Hadamard butterflies over a half-warp's 128 values in
+// double: this lane holds elements 8 sub .. 8 sub + 7.
+__device__ __forceinline__ void wht128_halfwarp(double (&x)[8], int sub, unsigned hmask) {
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if ((j & h) == 0) {
+                const double a = x[j], b = x[j + h];
+                x[j] = a + b;
+                x[j + h] = a - b;
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) {
+        const bool upper = (sub & m) != 0;   // this lane holds the "+ h" side of each pair
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const double p = __shfl_xor_sync(hmask, x[j], m, 16);
+            x[j] = upper ? p - x[j] : x[j] + p;
+        }
+    }
+}
+
+// bf16 bits of a float, round to nearest even (finite values).
+__device__ __forceinline__ uint32_t bf16_rne(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+template <bool kFp8, bool kRotate>
 __global__ void __launch_bounds__(256) store_keys_kernel(const uint4* __restrict__ k,
                                                          const int64_t* __restrict__ slots,
                                                          int64_t n, uint8_t* __restrict__ pool,
                                                          int64_t num_blocks, int bs,
-                                                         int64_t block_bytes, int32_t* status) {
+                                                         int64_t block_bytes, int32_t* status,
+                                                         double rot_scale) {
     const int sub = threadIdx.x & 15;                     // lane within the half-warp
     const unsigned hmask = 0xFFFFu << (threadIdx.x & 16);  // this half-warp's lanes
     const int64_t tok0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
@@ -48,16 +93,32 @@ __global__ void __launch_bounds__(256) store_keys_kernel(const uint4* __restrict
         const int64_t off = slot - blk * bs;
         uint8_t* base = pool + blk * block_bytes;
         const uint4 v = k[tok * 16 + sub];
-        if constexpr (!kFp8) {
-            reinterpret_cast<uint4*>(base + off * 256)[sub] = v;
-        } else {
-            float x[8];
+        float x[8];
+        {
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 x[2 * i] = __uint_as_float(w4[i] << 16);
                 x[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
             }
+        }
+        if constexpr (kRotate) {
+            double xd[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xd[i] = static_cast<double>(x[i]);
+            wht128_halfwarp(xd, sub, hmask);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = __double2float_rn(__dmul_rn(xd[i], rot_scale));
+        }
+        if constexpr (!kFp8) {
+            if constexpr (kRotate) {
+                const uint4 o = make_uint4(bf16_rne(x[0]) | (bf16_rne(x[1]) << 16), bf16_rne(x[2]) | (bf16_rne(x[3]) << 16),
+                                           bf16_rne(x[4]) | (bf16_rne(x[5]) << 16), bf16_rne(x[6]) | (bf16_rne(x[7]) << 16));
+                reinterpret_cast<uint4*>(base + off * 256)[sub] = o;
+            } else {
+                reinterpret_cast<uint4*>(base + off * 256)[sub] = v;
+            }
+        } else {
             float amax = 0.0f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
@@ -88,20 +149,18 @@ __global__ void __launch_bounds__(256) store_keys_kernel(const uint4* __restrict
 }  // namespace
 
 cudaError_t launch_store(const idx_cache* c, const void* k, const int64_t* slots, int64_t n,
-                         int32_t* status, cudaStream_t st) {
+                         int32_t* status, bool rotate, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
     const int64_t threads = n * 16;
     int64_t blocks = (threads + 255) / 256;
     const int64_t cap = static_cast<int64_t>(c->num_sms) * 8;
     if (blocks > cap) blocks = cap;
-    if (c->key_dtype == IDX_KEY_FP8_E4M3)
-        store_keys_kernel<true><<<static_cast<int>(blocks), 256, 0, st>>>(
-            static_cast<const uint4*>(k), slots, n, c->pool, c->num_blocks, c->block_size,
-            c->block_bytes, status);
-    else
-        store_keys_kernel<false><<<static_cast<int>(blocks), 256, 0, st>>>(
-            static_cast<const uint4*>(k), slots, n, c->pool, c->num_blocks, c->block_size,
-            c->block_bytes, status);
+    const double rs = 1.0 / std::sqrt(static_cast<double>(kHeadDim));   // the double nearest 1/sqrt(128)
+    const bool fp8 = c->key_dtype == IDX_KEY_FP8_E4M3;
+    auto kern = fp8 ? (rotate ? store_keys_kernel<true, true> : store_keys_kernel<true, false>)
+                    : (rotate ? store_keys_kernel<false, true> : store_keys_kernel<false, false>);
+    kern<<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<const uint4*>(k), slots, n, c->pool,
+                                                   c->num_blocks, c->block_size, c->block_bytes, status, rs);
     return cudaGetLastError();
 }
 

@@ -602,18 +602,34 @@ __device__ int block_topk_sorted(Each each, EachSlow each_slow, const uint32_t* 
     return min(k, nsort);
 }
 
-// Write a top-k row: buf[0, nout) as indices (and scores), the rest of the k
-// outputs as -1 (and -inf).  nout < 0 writes a whole -1 row.  All threads.
+// Physical pool slot of logical key s of a sequence (its block-table row
+// bt_row of mbps entries, bs tokens per block): bt_row[s / bs] * bs + s % bs,
+// the logical-to-physical translate (csa_translate_pack) of "DeepSeek-V4
+// index_topk=1024 sparse indexer can't recall verbatim lines", section "How
+// it was isolated".  -1 for s < 0 or a block past the row.
+__device__ __forceinline__ int64_t slot_of(const int32_t* bt_row, int mbps, int bs, int32_t s) {
+    if (s < 0) return -1;
+    const int bi = s / bs;
+    if (bi >= mbps) return -1;
+    return static_cast<int64_t>(__ldg(bt_row + bi)) * bs + (s - bi * bs);
+}
+
+// Write a top-k row: buf[0, nout) as indices (and scores, and slots through
+// the block-table row bt_row when out_slot is set), the rest of the k outputs
+// as -1 (and -inf, -1).  nout < 0 writes a whole -1 row.  All threads.
 __device__ __forceinline__ void write_topk_row(const uint64_t* buf, int nout, int k, int32_t* out_idx,
-                                               float* out_score) {
+                                               float* out_score, int64_t* out_slot = nullptr,
+                                               const int32_t* bt_row = nullptr, int mbps = 0, int bs = 1) {
     for (int j = threadIdx.x; j < k; j += blockDim.x) {
         if (j < nout) {
             const uint64_t c = buf[j];
             out_idx[j] = comp_index(c);
             if (out_score) out_score[j] = key_score(comp_key(c));
+            if (out_slot) out_slot[j] = slot_of(bt_row, mbps, bs, comp_index(c));
         } else {
             out_idx[j] = -1;
             if (out_score) out_score[j] = -INFINITY;
+            if (out_slot) out_slot[j] = -1;
         }
     }
 }

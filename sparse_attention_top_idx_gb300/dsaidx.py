@@ -54,18 +54,24 @@ def load(path: Optional[str] = None):
     L.idx_cache_destroy.restype = None
     L.idx_store_keys.argtypes = [P, P, P, I64, P, P]
     L.idx_store_keys.restype = I
+    L.idx_store_keys_rotated.argtypes = [P, P, P, I64, P, P]
+    L.idx_store_keys_rotated.restype = I
     L.idx_workspace_bytes_decode.argtypes = [P, I, I, I, I]
     L.idx_workspace_bytes_decode.restype = SZ
     L.idx_workspace_init.argtypes = [P, SZ, P]
     L.idx_workspace_init.restype = I
     L.idx_score_topk_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, P, P, P, SZ, P]
     L.idx_score_topk_decode.restype = I
+    L.idx_score_topk_decode_slots.argtypes = [P, P, P, P, I, P, I, I, I, I, P, P, P, P, SZ, P]
+    L.idx_score_topk_decode_slots.restype = I
     L.idx_score_topk_decode_static.argtypes = [P, P, P, P, I, P, I, I, I, I, P, P, P]
     L.idx_score_topk_decode_static.restype = I
     L.idx_workspace_bytes_prefill.argtypes = [P, I, I, I, I, I]
     L.idx_workspace_bytes_prefill.restype = SZ
     L.idx_score_topk_prefill.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, SZ, P]
     L.idx_score_topk_prefill.restype = I
+    L.idx_score_topk_prefill_slots.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, SZ, P]
+    L.idx_score_topk_prefill_slots.restype = I
     L.idx_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     L.idx_read_device_status.restype = I
     L.idx_status_str.argtypes = [I]
@@ -159,15 +165,17 @@ class IndexCache:
 
 
 def store_keys(cache: IndexCache, k_bf16: torch.Tensor, slot_mapping: torch.Tensor,
-               status: Optional[torch.Tensor] = None, stream=None):
-    """idx_store_keys: quantise (fp8) or copy (bf16) n keys into their slots."""
+               status: Optional[torch.Tensor] = None, stream=None, rotate: bool = False):
+    """idx_store_keys: quantise (fp8) or copy (bf16) n keys into their slots;
+    rotate=True: idx_store_keys_rotated (Walsh-Hadamard rotation first)."""
     n = k_bf16.shape[0]
     _need(k_bf16, torch.bfloat16, "k_bf16", (n, HEAD_DIM))
     _need(slot_mapping, torch.int64, "slot_mapping", (n,))
     if status is not None:
         _need(status, torch.int32, "status")
-    _check(load().idx_store_keys(cache.handle, _ptr(k_bf16), _ptr(slot_mapping), n, _ptr(status),
-                                 _stream(stream)), "idx_store_keys")
+    fn = load().idx_store_keys_rotated if rotate else load().idx_store_keys
+    name = "idx_store_keys_rotated" if rotate else "idx_store_keys"
+    _check(fn(cache.handle, _ptr(k_bf16), _ptr(slot_mapping), n, _ptr(status), _stream(stream)), name)
 
 
 def workspace_bytes_decode(cache: IndexCache, batch: int, max_seq_len: int, heads: int, topk: int) -> int:
@@ -178,7 +186,7 @@ def score_topk_decode_static(cache: IndexCache, q: torch.Tensor, w: torch.Tensor
                              seq_lens: torch.Tensor, max_seq_len: int, topk: int, out_idx: torch.Tensor,
                              out_score: Optional[torch.Tensor] = None, stream=None):
     """idx_score_topk_decode_static: decode without a workspace (the library's
-    own fixed 8 MiB scratch per GPU; calls must not overlap on the GPU)."""
+    own fixed 32 MiB scratch per GPU; calls must not overlap on the GPU)."""
     B, H = q.shape[0], q.shape[1]
     _need(q, torch.bfloat16, "q", (B, H, HEAD_DIM))
     _need(w, torch.float32, "w", (B, H))
@@ -214,8 +222,11 @@ def workspace_init(ws: torch.Tensor, stream=None):
 
 def score_topk_decode(cache: IndexCache, q: torch.Tensor, w: torch.Tensor, block_table: torch.Tensor,
                       seq_lens: torch.Tensor, max_seq_len: int, topk: int, out_idx: torch.Tensor,
-                      workspace: torch.Tensor, out_score: Optional[torch.Tensor] = None, stream=None):
-    """idx_score_topk_decode: one query per sequence, all its keys visible."""
+                      workspace: torch.Tensor, out_score: Optional[torch.Tensor] = None, stream=None,
+                      out_slot: Optional[torch.Tensor] = None):
+    """idx_score_topk_decode: one query per sequence, all its keys visible;
+    with out_slot ([batch, topk] int64) idx_score_topk_decode_slots, which
+    also writes each selected key's physical pool slot."""
     B, H = q.shape[0], q.shape[1]
     _need(q, torch.bfloat16, "q", (B, H, HEAD_DIM))
     _need(w, torch.float32, "w", (B, H))
@@ -227,6 +238,13 @@ def score_topk_decode(cache: IndexCache, q: torch.Tensor, w: torch.Tensor, block
     _need(workspace, torch.uint8, "workspace")
     if block_table.dim() != 2 or block_table.shape[0] != B:
         raise ValueError("block_table must be [batch, max_blocks_per_seq]")
+    if out_slot is not None:
+        _need(out_slot, torch.int64, "out_slot", (B, topk))
+        _check(load().idx_score_topk_decode_slots(cache.handle, _ptr(q), _ptr(w), _ptr(block_table),
+                                                  block_table.shape[1], _ptr(seq_lens), B, max_seq_len, H, topk,
+                                                  _ptr(out_idx), _ptr(out_score), _ptr(out_slot), _ptr(workspace),
+                                                  workspace.numel(), _stream(stream)), "idx_score_topk_decode_slots")
+        return
     _check(load().idx_score_topk_decode(cache.handle, _ptr(q), _ptr(w), _ptr(block_table),
                                         block_table.shape[1], _ptr(seq_lens), B, max_seq_len, H, topk,
                                         _ptr(out_idx), _ptr(out_score), _ptr(workspace), workspace.numel(),
@@ -236,8 +254,11 @@ def score_topk_decode(cache: IndexCache, q: torch.Tensor, w: torch.Tensor, block
 def score_topk_prefill(cache: IndexCache, q: torch.Tensor, w: torch.Tensor, cu_seqlens_q: torch.Tensor,
                        seq_lens: torch.Tensor, block_table: torch.Tensor, max_seq_len: int, topk: int,
                        out_idx: torch.Tensor, workspace: torch.Tensor,
-                       out_score: Optional[torch.Tensor] = None, stream=None):
-    """idx_score_topk_prefill: causal query chunks (queries at each sequence's last positions)."""
+                       out_score: Optional[torch.Tensor] = None, stream=None,
+                       out_slot: Optional[torch.Tensor] = None):
+    """idx_score_topk_prefill: causal query chunks (queries at each sequence's
+    last positions); with out_slot ([total_q, topk] int64)
+    idx_score_topk_prefill_slots."""
     T, H = q.shape[0], q.shape[1]
     B = seq_lens.shape[0]
     _need(q, torch.bfloat16, "q", (T, H, HEAD_DIM))
@@ -251,6 +272,14 @@ def score_topk_prefill(cache: IndexCache, q: torch.Tensor, w: torch.Tensor, cu_s
     _need(workspace, torch.uint8, "workspace")
     if block_table.dim() != 2 or block_table.shape[0] != B:
         raise ValueError("block_table must be [batch, max_blocks_per_seq]")
+    if out_slot is not None:
+        _need(out_slot, torch.int64, "out_slot", (T, topk))
+        _check(load().idx_score_topk_prefill_slots(cache.handle, _ptr(q), _ptr(w), _ptr(cu_seqlens_q),
+                                                   _ptr(seq_lens), _ptr(block_table), block_table.shape[1], B, T,
+                                                   max_seq_len, H, topk, _ptr(out_idx), _ptr(out_score),
+                                                   _ptr(out_slot), _ptr(workspace), workspace.numel(),
+                                                   _stream(stream)), "idx_score_topk_prefill_slots")
+        return
     _check(load().idx_score_topk_prefill(cache.handle, _ptr(q), _ptr(w), _ptr(cu_seqlens_q), _ptr(seq_lens),
                                          _ptr(block_table), block_table.shape[1], B, T, max_seq_len, H, topk,
                                          _ptr(out_idx), _ptr(out_score), _ptr(workspace), workspace.numel(),

@@ -231,3 +231,26 @@ def test_timeout_path_flags_rows_and_the_next_call_recovers():
     assert np.all(np.isneginf(got["score"]))
     again = run_decode(W, dsaidx.FP8, cache=cache)
     check(W, dsaidx.FP8, again)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_slot_output_is_the_block_table_translate(mode):
+    # idx_score_topk_decode_slots: out_slot equals the oracle's translate of the
+    # returned indices (bit for bit), -1 where out_idx is -1; one- and
+    # multi-segment rows, an empty row, blocks of 32 and 64
+    for bs in (32, 64):
+        W = wl.make_workload("slots", [3000, 70000, 0, 129], [1] * 4, topk=512, bs=bs, seed=71 + bs + mode)
+        cache = build_cache(W, mode)
+        ins = decode_inputs(W)
+        B, k = W.batch, W.topk
+        ws = dsaidx.new_workspace(dsaidx.workspace_bytes_decode(cache, B, W.max_seq_len, W.H, k))
+        oi = torch.full((B, k), -7, dtype=torch.int32, device="cuda")
+        osl = torch.full((B, k), -7, dtype=torch.int64, device="cuda")
+        dsaidx.score_topk_decode(cache, ins["q"], ins["w"], ins["block_table"], ins["seq_lens"], W.max_seq_len, k,
+                                 oi, ws, out_slot=osl)
+        idx, slots = oi.cpu().numpy(), osl.cpu().numpy()
+        ref = run_decode(W, mode, cache=cache)
+        assert np.array_equal(idx, ref["idx"])
+        for b in range(B):
+            assert np.array_equal(slots[b], oracle.translate_slots(W.block_table[b], bs, idx[b]))
+        assert np.all(slots[2] == -1)

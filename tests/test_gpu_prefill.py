@@ -4,6 +4,7 @@ prefill chunk at full size (sampled rows against the oracle, every row against
 the selection invariants), and decode / prefill agreement."""
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from sparse_attention_top_idx_gb300 import dsaidx
@@ -64,6 +65,44 @@ def test_prefill_chunk_full_size_sampled():
     assert np.all(np.diff(got["score"], axis=1) <= 0)     # descending in every row
 
 
+def test_prefill_chunk_full_size_dense_rows_and_scores():
+    # the full-size chunk (22000 keys, 8192 causal queries, top-1024): rows
+    # 4090..4200, the last 64 and every 4th row against the oracle -- the
+    # selections, and every visible fp32 score the scoring kernel left in the
+    # workspace (its layout: 256-byte header, one flag word per row rounded up
+    # to 256 bytes, then the score rows of max_seq_len rounded up to 4 floats)
+    from sparse_attention_top_idx_gb300.host import bf16_tensor
+    W = wl.prefill_chunk()
+    cache = build_cache(W, dsaidx.FP8)
+    T, k = W.total_q, W.topk
+    nbytes = dsaidx.workspace_bytes_prefill(cache, W.batch, T, W.max_seq_len, W.H, k)
+    ws = dsaidx.new_workspace(nbytes)
+    oi = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    osc = torch.full((T, k), float("nan"), dtype=torch.float32, device="cuda")
+    dsaidx.score_topk_prefill(cache, bf16_tensor(W.q), torch.from_numpy(W.w).cuda(),
+                              torch.from_numpy(W.cu_seqlens_q()).cuda(),
+                              torch.tensor(W.seq_lens, dtype=torch.int32, device="cuda"),
+                              torch.from_numpy(W.block_table).cuda(), W.max_seq_len, k, oi, ws, out_score=osc)
+    assert dsaidx.read_device_status(ws) == 0
+    got = {"idx": oi.cpu().numpy(), "score": osc.cpu().numpy()}
+    rows = sorted(set(list(range(4090, 4201)) + list(range(T - 64, T)) + list(range(0, T, 4))))
+    ref, nvis = oracle_ref(W, dsaidx.FP8, rows)
+    exact = check_rows(got, ref, nvis, W.topk, rows=rows)
+    assert exact >= len(rows) - 8
+    align = lambda x, a: (x + a - 1) // a * a
+    off = align(256 + T * 4, 256)
+    stride = align(W.max_seq_len, 4)
+    scores = ws[off: off + T * stride * 4].view(torch.float32).view(T, stride)
+    sub = scores[torch.tensor(rows, device="cuda")].cpu().numpy()
+    for i, r in enumerate(rows):
+        nv = int(nvis[i])
+        want = ref["scores"][i, :nv].astype(np.float64)
+        have = sub[i, :nv].astype(np.float64)
+        tol = 1e-3 * np.abs(want) + 1e-6 * np.abs(want).max()
+        bad = np.nonzero(np.abs(have - want) > tol)[0]
+        assert bad.size == 0, "row %d: %d of %d scores off, first at key %d" % (r, bad.size, nv, bad[0])
+
+
 @pytest.mark.parametrize("mode", [0, 1])
 def test_last_prefill_row_equals_decode(mode):
     # decode is the one-query chunk: same scores and selection for the last row
@@ -105,3 +144,22 @@ def test_kernel_timing_records_each_kernel():
     dsaidx.kernel_timing(0)
     run_decode(D, dsaidx.FP8)
     assert dsaidx.kernel_times() == []
+
+
+def test_prefill_slot_output_is_the_block_table_translate():
+    W = wl.make_workload("pslots", [2500, 300], [40, 7], topk=128, bs=32, seed=81)
+    cache = build_cache(W, dsaidx.FP8)
+    T, k = W.total_q, W.topk
+    from sparse_attention_top_idx_gb300.host import bf16_tensor
+    ws = dsaidx.new_workspace(dsaidx.workspace_bytes_prefill(cache, W.batch, T, W.max_seq_len, W.H, k))
+    oi = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    osl = torch.full((T, k), -7, dtype=torch.int64, device="cuda")
+    dsaidx.score_topk_prefill(cache, bf16_tensor(W.q), torch.from_numpy(W.w).cuda(),
+                              torch.from_numpy(W.cu_seqlens_q()).cuda(),
+                              torch.tensor(W.seq_lens, dtype=torch.int32, device="cuda"),
+                              torch.from_numpy(W.block_table).cuda(), W.max_seq_len, k, oi, ws, out_slot=osl)
+    idx, slots = oi.cpu().numpy(), osl.cpu().numpy()
+    ref = run_prefill(W, dsaidx.FP8, cache=cache)
+    assert np.array_equal(idx, ref["idx"])
+    for r, b in enumerate(W.row_seq()):
+        assert np.array_equal(slots[r], oracle.translate_slots(W.block_table[b], W.bs, idx[r]))

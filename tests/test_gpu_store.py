@@ -91,3 +91,54 @@ def test_out_of_range_slot_sets_status_and_skips():
     mask[:128] = mask[5 * 128:6 * 128] = False
     mask[8192:8196] = mask[8192 + 20:8192 + 24] = False
     assert np.all(pool[mask] == 0x11)
+
+
+@pytest.mark.parametrize("bs", [32, 64])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rotated_store_bit_exact(bs, mode):
+    # idx_store_keys_rotated against the oracle's rotated store, every byte
+    W = wl.make_workload("strot", [1000, 77, 64, 3000], [1, 1, 1, 1], bs=bs, seed=20 + bs + mode,
+                         extra_blocks=5)
+    k = W.all_keys().copy()
+    slots = W.all_slots().copy()
+    slots[::13] = -1
+    rng = np.random.default_rng(100 + bs + mode)
+    scale = (10.0 ** rng.uniform(-30, 30, (k.shape[0], 1))).astype(np.float32)
+    kf = wl.bf16_bits_to_f32(k) * scale
+    kf[7] = 0.0
+    kf[9] = 1.0                       # all-ones row: its energy moves to entry 0
+    k = wl.f32_to_bf16_bits(kf)
+    cache = dsaidx.IndexCache.allocate(W.num_blocks, bs, mode, fill=0xA5)
+    dsaidx.store_keys(cache, bf16_tensor(k), torch.from_numpy(slots).cuda(), rotate=True)
+    got = cache.pool.cpu().numpy()
+    bb = oracle.block_bytes(mode, W.bs)
+    want = np.full(W.num_blocks * bb, 0xA5, np.uint8)
+    oracle.store_keys(want, k, slots, W.bs, mode, rotate=True)
+    diff = np.nonzero(got != want)[0]
+    assert diff.size == 0, "first differing byte %d of %d" % (diff[0], diff.size)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rotated_keys_and_queries_score_parity(mode):
+    # keys stored rotated, queries rotated by the caller (here with the
+    # oracle's rotation, rounded to bf16): decode parity against the oracle on
+    # the same rotated operands, and the planted needle still ranks first
+    from tests.parity import check_rows, decode_inputs
+    W = wl.make_workload("rotdec", [3000, 9000, 129], [1, 1, 1], topk=256, seed=31 + mode)
+    B, H, d = W.q.shape
+    qr = oracle.f32_to_bf16(oracle.wht_rows(W.q.reshape(B * H, d))).reshape(B, H, d)
+    cache = dsaidx.IndexCache.allocate(W.num_blocks, W.bs, mode, fill=0)
+    dsaidx.store_keys(cache, bf16_tensor(W.all_keys()), torch.from_numpy(W.all_slots()).cuda(), rotate=True)
+    ins = decode_inputs(W)
+    ws = dsaidx.new_workspace(dsaidx.workspace_bytes_decode(cache, B, W.max_seq_len, H, W.topk))
+    oi = torch.full((B, W.topk), -7, dtype=torch.int32, device="cuda")
+    osc = torch.full((B, W.topk), float("nan"), dtype=torch.float32, device="cuda")
+    dsaidx.score_topk_decode(cache, bf16_tensor(qr), ins["w"], ins["block_table"], ins["seq_lens"],
+                             W.max_seq_len, W.topk, oi, ws, out_score=osc)
+    got = {"idx": oi.cpu().numpy(), "score": osc.cpu().numpy()}
+    keys = [oracle.rotated_key_rows(W.keys[b], mode) for b in range(B)]
+    pos = np.asarray(W.seq_lens, np.int64) - 1
+    ref = oracle.score_topk(mode, W.topk, qr, W.w, np.arange(B, dtype=np.int32), pos, keys, full_scores=True)
+    check_rows(got, ref, pos + 1, W.topk)
+    for b in range(B):
+        assert got["idx"][b][0] == W.needle_pos[b]

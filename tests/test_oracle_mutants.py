@@ -39,6 +39,8 @@ MUTANTS = {
     "wht_index_or": ("s += orc_odd_parity((unsigned)(i & j)) ? -v : v;",
                      "s += orc_odd_parity((unsigned)(i | j)) ? -v : v;"),
     "bf16_round_half_up": ("u = u + 0x7FFFu + ((u >> 16) & 1u);", "u = u + 0x8000u;"),
+    "translate_offset_dropped": ("out[i] = (int64_t)table_row[s / bs] * bs + s % bs;",
+                                 "out[i] = (int64_t)table_row[s / bs] * bs;"),
 }
 
 
@@ -115,6 +117,12 @@ def battery(O) -> bool:
     c1, s1 = O.quantize_rows(Wk.keys[0])
     if not (np.array_equal(c1, c2) and np.array_equal(s1, s2)):
         return False
+    # translate: the slot of logical index s holds the gathered key s
+    sl = O.translate_slots(Wk.block_table[0], 64, np.arange(100, dtype=np.int32))
+    for s_, slot in enumerate(sl):
+        blk, off = divmod(int(slot), 64)
+        if not np.array_equal(pool[blk * 8448 + off * 128: blk * 8448 + off * 128 + 128], c2[s_]):
+            return False
     return True
 
 

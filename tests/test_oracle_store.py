@@ -78,3 +78,32 @@ def test_store_rejects_out_of_range_slot():
     k = np.zeros((1, 128), np.uint16)
     with pytest.raises(ValueError):
         oracle.store_keys(pool, k, np.array([64], np.int64), 64, oracle.FP8)
+
+
+@pytest.mark.parametrize("bs", [32, 64])
+@pytest.mark.parametrize("dtype", [oracle.FP8, oracle.BF16])
+def test_translate_is_the_block_table_gather(bs, dtype):
+    # the token at physical slot translate(s) is the key the block-table gather
+    # returns for logical index s (ROCm/ATOM #1507, "How it was isolated": the
+    # translate feeds sparse attention the rows the indexer selected)
+    W = wl.make_workload("tr", [700, 129], [1, 1], bs=bs, seed=61 + bs + dtype, extra_blocks=3)
+    bb = oracle.block_bytes(dtype, bs)
+    pool = np.zeros(W.num_blocks * bb, np.uint8)
+    oracle.store_keys(pool, W.all_keys(), W.all_slots(), bs, dtype)
+    for b in range(W.batch):
+        S = W.seq_lens[b]
+        idx = np.concatenate([np.arange(S), [-1, -1]]).astype(np.int32)
+        slots = oracle.translate_slots(W.block_table[b], bs, idx)
+        assert np.all(slots[-2:] == -1)
+        g = oracle.gather_keys(pool, W.block_table[b], S, bs, dtype)
+        for s, sl in zip(idx[:-2], slots[:-2]):
+            blk, off = divmod(int(sl), bs)
+            base = blk * bb
+            if dtype == oracle.FP8:
+                codes = pool[base + off * 128: base + off * 128 + 128]
+                scale = pool[base + bs * 128 + off * 4: base + bs * 128 + off * 4 + 4].view(np.float32)[0]
+                assert np.array_equal(codes, g[0][s]) and scale == g[1][s]
+            else:
+                assert np.array_equal(pool[base + off * 256: base + off * 256 + 256].view(np.uint16), g[s])
+    # an index whose block lies past the table row
+    assert oracle.translate_slots(np.array([3, 4], np.int32), bs, np.array([2 * bs], np.int32))[0] == -1
