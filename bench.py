@@ -44,9 +44,9 @@ N_POOL_COPIES = 9
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources they were taken on; a stale hash reports null.
 NCU_TRAFFIC = {
-    ("decode", "43edacfe482c8e12"): 31459072 + 0,
-    ("longctx", "43edacfe482c8e12"): 277265664 + 2918912,
-    ("prefill", "43edacfe482c8e12"): 140015104 + 528819456,   # the scoring kernel
+    ("decode", "4bac25815ef3aefd"): 31435776 + 0,
+    ("longctx", "4bac25815ef3aefd"): 277225984 + 2748672,
+    ("prefill", "4bac25815ef3aefd"): 140061184 + 531488256,   # the scoring kernel
 }
 
 

@@ -106,7 +106,8 @@ size_t idx_block_bytes(int key_dtype, int block_size, int head_dim);
 idx_status idx_cache_create(idx_cache** out, void* pool_dev, int64_t num_blocks,
                             int block_size, int head_dim, int key_dtype);
 
-/* Release a handle (host memory only; the pool is untouched).  NULL is a no-op. */
+/* Release a handle (host memory only; the pool is untouched).  NULL is a
+ * no-op.  (Library utility; no passage.) */
 void idx_cache_destroy(idx_cache* cache);
 
 /*
@@ -147,7 +148,8 @@ idx_status idx_store_keys_rotated(const idx_cache* cache, const void* k_bf16_dev
 
 /*
  * Workspace bytes a decode call needs for this batch shape (depends on the
- * handle's device and key format).  0 on invalid arguments.
+ * handle's device and key format).  0 on invalid arguments.  (Library
+ * utility; no passage: the pages' kernels allocate their own scratch.)
  */
 size_t idx_workspace_bytes_decode(const idx_cache* cache, int batch, int max_seq_len,
                                   int heads, int topk);
@@ -155,7 +157,7 @@ size_t idx_workspace_bytes_decode(const idx_cache* cache, int batch, int max_seq
 /*
  * Zero a newly allocated workspace (required once before its first use, and
  * again after any call that reported a device error).  The score calls leave
- * the workspace ready for the next call.
+ * the workspace ready for the next call.  (Library utility; no passage.)
  */
 idx_status idx_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream);
 
@@ -237,7 +239,8 @@ idx_status idx_score_topk_decode_static(const idx_cache* cache, const void* q_bf
                                         int batch, int max_seq_len, int heads, int topk,
                                         int32_t* out_idx_dev, float* out_score_dev, void* stream);
 
-/* Workspace bytes a prefill call needs.  0 on invalid arguments. */
+/* Workspace bytes a prefill call needs.  0 on invalid arguments.  (Library
+ * utility; no passage.) */
 size_t idx_workspace_bytes_prefill(const idx_cache* cache, int batch, int total_q,
                                    int max_seq_len, int heads, int topk);
 
@@ -277,7 +280,8 @@ idx_status idx_score_topk_prefill_slots(const idx_cache* cache, const void* q_bf
 /*
  * Synchronise `stream` and read the device status word of a workspace into
  * *code_out (IDX_OK, IDX_ERR_DEVICE_CHECK or IDX_ERR_TIMEOUT).  For tests and
- * debugging; the status stays set until idx_workspace_init.
+ * debugging; the status stays set until idx_workspace_init.  (Library
+ * utility; no passage.)
  */
 idx_status idx_read_device_status(const void* workspace_dev, void* stream, int32_t* code_out);
 

@@ -3,6 +3,7 @@
 // flags and the candidate buffer that idx_score_topk_decode keeps in the
 // caller's workspace) lives in a fixed array in the library's own device
 // memory instead, so the caller passes only inputs and outputs.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -18,24 +19,51 @@ constexpr size_t kStaticScratchBytes = static_cast<size_t>(32) << 20;   // 32 Mi
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
-// Device address of g_decode_scratch, per device.  In host code the array's
-// name is only a host-side stand-in, so the address is looked up once per
-// device (with that device current) and cached.
+// Device address of g_decode_scratch, per device and context.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// (with that device current) and cached together with the context it was
+// looked up in: a context that was destroyed and created again on the device
+// (cudaDeviceReset, for instance) has its module loaded anew, so a different
+// current context looks the address up again.
 std::mutex g_scratch_mu;
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+    CUcontext ctx = nullptr;
+    void* addr = nullptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    }
+    return fn;
+}
 
 idx_status scratch_of_current_device(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return IDX_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    CUcontext ctx = nullptr;
+    CtxGetCurrentFn get = ctx_get_current();
+    if (get == nullptr || get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+    ScratchAddr& e = g_scratch_addr[dev];
+    if (e.addr == nullptr || e.ctx != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return IDX_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        e.addr = p;
+        e.ctx = ctx;
     }
-    *out = g_scratch_addr[dev];
+    *out = e.addr;
     return IDX_OK;
 }
 
