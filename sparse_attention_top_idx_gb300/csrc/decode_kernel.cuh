@@ -87,7 +87,7 @@ struct DecShared {
     uint32_t scan[kThreads / 32];
     SegSelSmem sel;
 };
-static_assert(sizeof(DecShared) <= 4096, "DecShared must fit the misc region");
+static_assert(sizeof(DecShared) <= kDecMiscBytes, "DecShared must fit the misc region");
 
 template <bool kFp8, int kBs>
 __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorMap tmap, const ScoreParams p) {
@@ -635,6 +635,8 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
             const int32_t* btr = p.block_table + static_cast<int64_t>(b) * p.mbps;
             uint64_t* run_out = single ? nullptr : p.cand + static_cast<int64_t>(b) * p.cand_cap + static_cast<int64_t>(seg) * k;
             uint32_t* gh = single ? nullptr : p.ghist + static_cast<int64_t>(b) * kGHistWords;
+            // (runs: the fast path adds the run's bin counts from its tables after
+            // the ranks, one atomic per bin; the slow path one per winner)
             auto emit = [&](int r, uint64_t c) {
                 if (single) {
                     oi[r] = comp_index(c);
@@ -642,9 +644,11 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                     if (osl) osl[r] = slot_of(btr, p.mbps, kBs, comp_index(c));
                 } else {
                     run_out[r] = c;
-                    const uint32_t wb = win_bin(comp_key(c));
-                    atomicAdd(gh + wb, 1u);
-                    if (r == 0) atomicMax(gh + kGHistBins, wb + 1u);   // the sequence's largest bin (+1)
+                    if (!fast) {
+                        const uint32_t wb = win_bin(comp_key(c));
+                        atomicAdd(gh + wb, 1u);
+                        if (r == 0) atomicMax(gh + kGHistBins, wb + 1u);   // the sequence's largest bin (+1)
+                    }
                 }
             };
             if (flag) {
@@ -708,6 +712,16 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                         int rk = s0;
                         for (int j = s0; j < e0; ++j) rk += pool[j] > x ? 1 : 0;
                         if (rk < nsel) emit(rk, x);
+                    }
+                    if (!single && rank == lead) {
+                        // the run's entries per bin: every entry of a bin above the
+                        // boundary, the boundary bin's first nsel - start
+                        for (int t = bstar - wlo + tid; t < kWinBins; t += kThreads) {
+                            const int start = static_cast<int>(bstart[t]);
+                            const int c = t == bstar - wlo ? nsel - start : static_cast<int>(blen[t]);
+                            if (c > 0) atomicAdd(gh + wlo + t, static_cast<uint32_t>(c));
+                        }
+                        if (tid == 0) atomicMax(gh + kGHistBins, static_cast<uint32_t>(gmax) + 1u);
                     }
                 } else {
                     flag = 1;   // (a wait that ran out: the status word says so)

@@ -99,38 +99,37 @@ __host__ __device__ inline int dec_units(int S, int max_seq_len) {
     return (S > 0 && S <= max_seq_len) ? dec_nseg(S) : 1;
 }
 
-// Shared-memory plan of the decode kernel: the key stages (after the stream:
-// the selection's candidate lists and scratch); one region that holds in turn
-// the staged bf16 query rows, the chunk's 16-bit histogram (during the
-// stream) and the pool of every CTA's sorted candidates (during the
-// selection); the chunk's scores; the cluster's histogram windows; the B
-// tile, w', block ids, scratch and barriers.  fp8: about 99 KB, two CTAs per
-// SM; bf16: one.
+// Shared-memory plan of the decode kernel: three key stages (after the
+// stream: the selection's scratch), the B tile right after them (1024-byte
+// aligned for the 128-byte swizzle), one region that holds in turn this CTA's
+// staged bf16 query rows and the chunk's 16-bit histogram (during the stream)
+// and the pool of every CTA's candidates (during the selection), the chunk's
+// scores, the cluster's histogram windows, w', block ids, scratch and
+// barriers.  fp8: 114,832 bytes, two CTAs per SM; bf16: one.
 struct DecPlan {
     int stages, a_stage_bytes, a_off, raw_off, sc_off, win_off, pool_off, q_off, w_off, bid_off, misc_off, bar_off,
         total;
 };
+constexpr int kDecMiscBytes = 1536;
 __host__ __device__ inline DecPlan dec_plan(bool fp8) {
     DecPlan p{};
-    p.stages = 2;
+    p.stages = 3;
     p.a_stage_bytes = fp8 ? 16384 : 32768;
     int o = 0;
     p.a_off = o;      o += p.stages * p.a_stage_bytes;
-    p.raw_off = o;    o += 64 * 256 + 64 * 4;          // >= the 16 KB histogram and the 16 KB pool
+    p.q_off = o;      o += 64 * (fp8 ? 128 : 256);
+    p.raw_off = o;    o += 16384;                      // 2 KB query rows + w / 16 KB histogram / 16 KB pool
     p.pool_off = p.raw_off;
     p.sc_off = o;     o += kDecChunkMax * 4 + 16;
     p.win_off = o;    o += kDecCl * 528;
-    o = (o + 1023) / 1024 * 1024;
-    p.q_off = o;      o += 64 * (fp8 ? 128 : 256);
     p.w_off = o;      o += 64 * 4;
-    p.bid_off = o;    o += kDecChunkMax / 32 * 4;   // block ids of one chunk
-    p.misc_off = o;   o += 4096;
+    p.bid_off = o;    o += kDecChunkMax / 32 * 4;      // block ids of one chunk
+    p.misc_off = o;   o += kDecMiscBytes;
     p.bar_off = o;    o += 256;
     p.total = o + 1024;
     return p;
 }
-static_assert(2 * 16384 >= 4096 * 8, "the selection buffer fits the fp8 key stages");
-static_assert(kDecChunkMax * 4 >= 4096 * 4, "the selection histogram fits the chunk's score area");
+static_assert(3 * 16384 >= 4096 * 4 + 4096 * 8, "the selection scratch fits the fp8 key stages");
 constexpr int kDecMaxClusters(int sms) { return 2 * sms / kDecCl; }   // two CTAs per SM at most
 
 // Shared-memory plan of the prefill scoring kernel (kPrefillQT queries per
