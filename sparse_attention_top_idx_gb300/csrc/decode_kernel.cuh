@@ -706,77 +706,13 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                     // of its own bin
                     const int lo = static_cast<int>(rank) * ctot / kDecCl;
                     const int hi = (static_cast<int>(rank) + 1) * ctot / kDecCl;
-                    // entries of small bins (rank = the bin's start plus the larger
-                    // entries of the bin), each by the CTA that holds its pool slot
-                    constexpr int kCrowd = 256;
-                    for (int i = lo + tid; i < hi; i += kThreads) {
-                        const uint64_t x = pool[i];
-                        const int t = static_cast<int>(win_bin(comp_key(x))) - wlo;
-                        const int s0 = static_cast<int>(bstart[t]), e0 = s0 + static_cast<int>(blen[t]);
-                        if (e0 - s0 > kCrowd) continue;
-                        int rk = s0;
-                        for (int j = s0; j < e0; ++j) rk += pool[j] > x ? 1 : 0;
-                        if (rk < nsel) emit(rk, x);
-                    }
-                    // crowded bins reaching into this CTA's eighth: the bin is sorted by
-                    // counting on the next 8 key bits (256 sub-bins of a few entries),
-                    // ranks inside a sub-bin by comparison; this CTA writes the ranks
-                    // that fall in its eighth
                     {
                         uint32_t* scnt = bfill + kWinBins;                             // [256] sub-bin counts
                         uint32_t* scur = scnt + 256;                                   // [256] sub-bin cursors
-                        uint64_t* srt = reinterpret_cast<uint64_t*>(scur + 256);      // [<= 2048] the bin, by sub-bin
-                        auto sub = [](uint64_t c) { return (comp_key(c) >> (kWinShift - 8)) & 0xFFu; };
-                        // the crowded bins that reach into this eighth, one thread per bin
-                        uint32_t* clist = reinterpret_cast<uint32_t*>(srt + 2048);   // [<= 256]
-                        if (tid == 0) ks->nmine = 0u;
-                        __syncthreads();
-                        {
-                            const int t = tid;
-                            const int s0 = static_cast<int>(bstart[t]), len = static_cast<int>(blen[t]);
-                            if (t >= bstar - wlo && len > kCrowd && s0 < hi && s0 + len > lo)
-                                clist[atomicAdd(&ks->nmine, 1u)] = static_cast<uint32_t>(t);
-                        }
-                        __syncthreads();
-                        const int ncrowd = static_cast<int>(ks->nmine);
-                        for (int ci = 0; ci < ncrowd; ++ci) {
-                            const int t = static_cast<int>(clist[ci]);
-                            const int s0 = static_cast<int>(bstart[t]), len = static_cast<int>(blen[t]);
-                            scnt[tid] = 0u;
-                            __syncthreads();
-                            for (int j = tid; j < len; j += kThreads) atomicAdd(&scnt[sub(pool[s0 + j])], 1u);
-                            __syncthreads();
-                            // sub-bin tid starts after every entry of the higher sub-bins
-                            const uint32_t v = scnt[tid];
-                            uint32_t incl = v;
-#pragma unroll
-                            for (int o = 1; o < 32; o <<= 1) {
-                                const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
-                                if (lane + o < 32) incl += y;
-                            }
-                            if (lane == 0) ks->sel.wcnt[warp] = incl;
-                            __syncthreads();
-                            uint32_t start = incl - v;
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) start += q > warp ? ks->sel.wcnt[q] : 0u;
-                            scur[tid] = start;
-                            __syncthreads();
-                            for (int j = tid; j < len; j += kThreads) {
-                                const uint64_t y = pool[s0 + j];
-                                srt[atomicAdd(&scur[sub(y)], 1u)] = y;
-                            }
-                            __syncthreads();
-                            for (int q = tid; q < len; q += kThreads) {
-                                const uint64_t y = srt[q];
-                                const uint32_t u = sub(y);
-                                const int en = static_cast<int>(scur[u]), st = en - static_cast<int>(scnt[u]);
-                                int fp = st;
-                                for (int z = st; z < en; ++z) fp += srt[z] > y ? 1 : 0;
-                                const int rk = s0 + fp;
-                                if (rk >= lo && rk < hi && rk < nsel) emit(rk, y);
-                            }
-                            __syncthreads();
-                        }
+                        uint64_t* srt = reinterpret_cast<uint64_t*>(scur + 256);      // [2048] a crowded bin, by sub-bin
+                        uint32_t* clist = reinterpret_cast<uint32_t*>(srt + 2048);     // [256] crowded bins
+                        rank_pool(pool, lo, hi, nsel, bstar - wlo, wlo, bstart, blen, scnt, scur, clist, srt,
+                                  &ks->nmine, ks->sel.wcnt, emit);
                     }
                     if (!single && rank == lead) {
                         // the run's entries per bin: every entry of a bin above the

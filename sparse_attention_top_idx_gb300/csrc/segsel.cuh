@@ -401,6 +401,84 @@ constexpr int kCountSortMax = 96;                    // longest candidate list s
 __device__ __forceinline__ uint32_t win_bin(uint32_t key) { return key >> kWinShift; }
 
 
+// Ranks of the candidates of a bin-major pool, for the rank positions
+// [lo, hi) of one CTA: pool[0, ctot) holds the bins from the top down (bin
+// index t = (key >> kWinShift) - wlo; bin t's entries, in any order, at
+// [bstart[t], bstart[t] + blen[t])), tb is the lowest bin index with
+// candidates.  emit(r, c) is called once for each rank r < nsel in [lo, hi):
+// an entry of a bin of at most kRankCrowd entries by the CTA whose [lo, hi)
+// holds its pool slot (rank = bstart plus the larger entries of the bin); a
+// crowded bin is sorted by counting on the next 8 key bits (256 sub-bins of a
+// few entries, ranks inside a sub-bin by comparison) by every CTA whose
+// [lo, hi) it reaches, each emitting the ranks in its range.  Scratch: scnt,
+// scur, clist 256 words each, srt 2048 composites, counter one word, wcnt 8
+// words.  All 256 threads.
+constexpr int kRankCrowd = 128;
+template <class Emit>
+__device__ __forceinline__ void rank_pool(const uint64_t* pool, int lo, int hi, int nsel, int tb, int wlo,
+                                          const uint32_t* bstart, const uint32_t* blen, uint32_t* scnt,
+                                          uint32_t* scur, uint32_t* clist, uint64_t* srt, uint32_t* counter,
+                                          uint32_t* wcnt, Emit emit) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = lo + tid; i < hi; i += kTopkThreads) {
+        const uint64_t x = pool[i];
+        const int t = static_cast<int>(win_bin(comp_key(x))) - wlo;
+        const int s0 = static_cast<int>(bstart[t]), e0 = s0 + static_cast<int>(blen[t]);
+        if (e0 - s0 > kRankCrowd) continue;
+        int rk = s0;
+        for (int j = s0; j < e0; ++j) rk += pool[j] > x ? 1 : 0;
+        if (rk < nsel) emit(rk, x);
+    }
+    auto sub = [](uint64_t c) { return (comp_key(c) >> (kWinShift - 8)) & 0xFFu; };
+    if (tid == 0) *counter = 0u;
+    __syncthreads();
+    {
+        const int t = tid;
+        const int s0 = static_cast<int>(bstart[t]), len = static_cast<int>(blen[t]);
+        if (t >= tb && len > kRankCrowd && s0 < hi && s0 + len > lo) clist[atomicAdd(counter, 1u)] = static_cast<uint32_t>(t);
+    }
+    __syncthreads();
+    const int ncrowd = static_cast<int>(*counter);
+    for (int ci = 0; ci < ncrowd; ++ci) {
+        const int t = static_cast<int>(clist[ci]);
+        const int s0 = static_cast<int>(bstart[t]), len = static_cast<int>(blen[t]);
+        scnt[tid] = 0u;
+        __syncthreads();
+        for (int j = tid; j < len; j += kTopkThreads) atomicAdd(&scnt[sub(pool[s0 + j])], 1u);
+        __syncthreads();
+        // sub-bin tid starts after every entry of the higher sub-bins
+        const uint32_t v = scnt[tid];
+        uint32_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+            if (lane + o < 32) incl += y;
+        }
+        if (lane == 0) wcnt[warp] = incl;
+        __syncthreads();
+        uint32_t start = incl - v;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) start += q > warp ? wcnt[q] : 0u;
+        scur[tid] = start;
+        __syncthreads();
+        for (int j = tid; j < len; j += kTopkThreads) {
+            const uint64_t y = pool[s0 + j];
+            srt[atomicAdd(&scur[sub(y)], 1u)] = y;
+        }
+        __syncthreads();
+        for (int q = tid; q < len; q += kTopkThreads) {
+            const uint64_t y = srt[q];
+            const uint32_t u = sub(y);
+            const int en = static_cast<int>(scur[u]), st = en - static_cast<int>(scnt[u]);
+            int fp = st;
+            for (int z = st; z < en; ++z) fp += srt[z] > y ? 1 : 0;
+            const int rk = s0 + fp;
+            if (rk >= lo && rk < hi && rk < nsel) emit(rk, y);
+        }
+        __syncthreads();
+    }
+}
+
 // Exact sorted top-k over the nseg sorted runs of k composites (zero-padded)
 // of one sequence, runs[j * k + e] in global memory, given the histogram gh
 // (kGHistWords words: kGHistBins bins of key >> 19 over every run entry, then
