@@ -147,6 +147,28 @@ idx_status idx_store_keys_rotated(const idx_cache* cache, const void* k_bf16_dev
                                   int32_t* status_dev, void* stream);
 
 /*
+ * Gather read of the cache (cp_gather_indexer_k_quant_cache in "DeepSeek-V4
+ * index_topk=1024 sparse indexer can't recall verbatim lines", ROCm/ATOM issue
+ * #1507, section "How it was isolated", where a gathered copy cross-checks
+ * the paged read): copies, byte for byte, every block that holds keys of a
+ * sequence into a caller-owned dense grid of blocks -- block j of sequence b
+ * (j < ceil(seq_lens[b] / block_size)) from block_table[b][j] to
+ * dst_pool_dev + (b * max_blocks_per_seq + j) * idx_block_bytes().
+ *  dst_pool_dev: batch * max_blocks_per_seq blocks, 16-byte aligned; blocks
+ *                past a sequence's end are not written.  The grid is itself a
+ *                pool: bound to a handle with the identity block table
+ *                (row b: b * max_blocks_per_seq + j) the score calls read
+ *                the same keys contiguously.
+ *  status_dev:   nullable device int32, set to IDX_ERR_DEVICE_CHECK when a
+ *                block id lies outside the pool (that block is skipped).
+ * Errors: IDX_ERR_INVALID_ARG (null or misaligned pointers, other device),
+ * IDX_ERR_CUDA (launch).
+ */
+idx_status idx_gather_blocks(const idx_cache* cache, const int32_t* block_table_dev,
+                             int max_blocks_per_seq, const int32_t* seq_lens_dev, int batch,
+                             void* dst_pool_dev, int32_t* status_dev, void* stream);
+
+/*
  * Workspace bytes a decode call needs for this batch shape (depends on the
  * handle's device and key format).  0 on invalid arguments.  (Library
  * utility; no passage: the pages' kernels allocate their own scratch.)

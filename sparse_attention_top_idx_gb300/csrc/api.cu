@@ -176,6 +176,18 @@ idx_status idx_store_keys_rotated(const idx_cache* cache, const void* k_bf16_dev
     return store_keys_common(cache, k_bf16_dev, slot_mapping_dev, n, status_dev, true, stream);
 }
 
+idx_status idx_gather_blocks(const idx_cache* cache, const int32_t* block_table_dev, int max_blocks_per_seq,
+                             const int32_t* seq_lens_dev, int batch, void* dst_pool_dev, int32_t* status_dev,
+                             void* stream) {
+    if (!cache || batch < 0 || max_blocks_per_seq < 1) return IDX_ERR_INVALID_ARG;
+    if (batch == 0) return IDX_OK;
+    if (!block_table_dev || !seq_lens_dev || !dst_pool_dev || !aligned(dst_pool_dev, 16)) return IDX_ERR_INVALID_ARG;
+    if (!same_device(cache)) return IDX_ERR_INVALID_ARG;
+    cudaError_t e = dsaidx::launch_gather(cache, block_table_dev, max_blocks_per_seq, seq_lens_dev, batch,
+                                          dst_pool_dev, status_dev, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
 size_t idx_workspace_bytes_decode(const idx_cache* cache, int batch, int max_seq_len, int heads, int topk) {
     if (!cache || batch < 0 || max_seq_len < 0 || heads != dsaidx::kHeads) return 0;
     if (topk < 1 || topk > IDX_MAX_TOPK) return 0;

@@ -180,6 +180,8 @@ cudaError_t launch_store(const idx_cache* c, const void* k, const int64_t* slots
                          int32_t* status, bool rotate, cudaStream_t st);
 cudaError_t launch_decode(const idx_cache* c, const ScoreParams& p, cudaStream_t st);
 cudaError_t launch_prefill(const idx_cache* c, const ScoreParams& p, cudaStream_t st);
+cudaError_t launch_gather(const idx_cache* c, const int32_t* block_table, int mbps, const int32_t* seq_lens,
+                          int batch, void* dst, int32_t* status, cudaStream_t st);
 // Per-kernel timing hook (ktimer.cu): records the next event when timing is on.
 void kt_mark(cudaStream_t st);
 

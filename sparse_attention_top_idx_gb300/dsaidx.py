@@ -56,6 +56,8 @@ def load(path: Optional[str] = None):
     L.idx_store_keys.restype = I
     L.idx_store_keys_rotated.argtypes = [P, P, P, I64, P, P]
     L.idx_store_keys_rotated.restype = I
+    L.idx_gather_blocks.argtypes = [P, P, I, P, I, P, P, P]
+    L.idx_gather_blocks.restype = I
     L.idx_workspace_bytes_decode.argtypes = [P, I, I, I, I]
     L.idx_workspace_bytes_decode.restype = SZ
     L.idx_workspace_init.argtypes = [P, SZ, P]
@@ -176,6 +178,22 @@ def store_keys(cache: IndexCache, k_bf16: torch.Tensor, slot_mapping: torch.Tens
     fn = load().idx_store_keys_rotated if rotate else load().idx_store_keys
     name = "idx_store_keys_rotated" if rotate else "idx_store_keys"
     _check(fn(cache.handle, _ptr(k_bf16), _ptr(slot_mapping), n, _ptr(status), _stream(stream)), name)
+
+
+def gather_blocks(cache: IndexCache, block_table: torch.Tensor, seq_lens: torch.Tensor, dst: torch.Tensor,
+                  status: Optional[torch.Tensor] = None, stream=None):
+    """idx_gather_blocks: copy every sequence's blocks, in logical order, into
+    the dense grid dst ([batch * max_blocks_per_seq] blocks, uint8)."""
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(dst, torch.uint8, "dst")
+    B, mbps = block_table.shape
+    if dst.numel() < B * mbps * block_bytes(cache.key_dtype, cache.block_size):
+        raise ValueError("dst must hold batch * max_blocks_per_seq blocks")
+    if status is not None:
+        _need(status, torch.int32, "status")
+    _check(load().idx_gather_blocks(cache.handle, _ptr(block_table), mbps, _ptr(seq_lens), B, _ptr(dst),
+                                    _ptr(status), _stream(stream)), "idx_gather_blocks")
 
 
 def workspace_bytes_decode(cache: IndexCache, batch: int, max_seq_len: int, heads: int, topk: int) -> int:
