@@ -44,9 +44,9 @@ N_POOL_COPIES = 9
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources they were taken on; a stale hash reports null.
 NCU_TRAFFIC = {
-    ("decode", "4bac25815ef3aefd"): 31435776 + 0,
-    ("longctx", "4bac25815ef3aefd"): 277225984 + 2748672,
-    ("prefill", "4bac25815ef3aefd"): 140061184 + 531488256,   # the scoring kernel
+    ("decode", "50fe28e59007d687"): 31443968 + 0,
+    ("longctx", "50fe28e59007d687"): 277238272 + 2797312,
+    ("prefill", "50fe28e59007d687"): 139622144 + 531330560,   # the scoring kernel
 }
 
 

@@ -51,9 +51,9 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def _compile(src: str) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc()] + ARCH + NVCC_FLAGS + ["-c", src, "-o", obj]
+def _compile(src: str, build_dir: str = BUILD, extra=()) -> tuple[str, str]:
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc()] + ARCH + NVCC_FLAGS + list(extra) + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, r.stdout, r.stderr))
@@ -80,6 +80,28 @@ def build(force: bool = False, verbose: bool = False) -> str:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
     os.replace(tmp, LIB)
     return LIB
+
+
+PHASES_LIB = os.path.join(HERE, "libdsaidx_phases.so")
+
+
+def build_phases() -> str:
+    """The diagnostic variant libdsaidx_phases.so: the same sources compiled
+    with -DDSAIDX_PHASE_STAMPS (the decode kernel records %globaltimer at its
+    phase boundaries).  Not part of the product build."""
+    bdir = os.path.join(HERE, "_build_phases")
+    if os.path.exists(PHASES_LIB) and all(os.path.getmtime(d) <= os.path.getmtime(PHASES_LIB) for d in _deps()):
+        return PHASES_LIB
+    os.makedirs(bdir, exist_ok=True)
+    srcs = _sources()
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
+        results = list(ex.map(lambda src: _compile(src, bdir, ["-DDSAIDX_PHASE_STAMPS"]), srcs))
+    tmp = PHASES_LIB + ".tmp.%d" % os.getpid()
+    r = subprocess.run([nvcc()] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
+    os.replace(tmp, PHASES_LIB)
+    return PHASES_LIB
 
 
 def build_peak(force: bool = False) -> str:

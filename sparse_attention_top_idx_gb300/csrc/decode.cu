@@ -113,3 +113,17 @@ cudaError_t launch_decode(const idx_cache* c, const ScoreParams& p, cudaStream_t
 }
 
 }  // namespace dsaidx
+
+#ifdef DSAIDX_PHASE_STAMPS
+// Diagnostic build only: copies the phase stamps (kPhaseCtas x kPhaseUnits x
+// kPhaseSlots nanosecond values, 0 = not reached) to host memory `out` and,
+// with clear != 0, zeroes them on the device.  Returns 0 on success.
+extern "C" int idx_phase_stamps(unsigned long long* out, int clear) {
+    if (out && cudaMemcpyFromSymbol(out, dsaidx::g_phase, sizeof(dsaidx::g_phase)) != cudaSuccess) return 1;
+    if (clear) {
+        static unsigned long long zero[dsaidx::kPhaseCtas][dsaidx::kPhaseUnits][dsaidx::kPhaseSlots];
+        if (cudaMemcpyToSymbol(dsaidx::g_phase, zero, sizeof(zero)) != cudaSuccess) return 1;
+    }
+    return 0;
+}
+#endif

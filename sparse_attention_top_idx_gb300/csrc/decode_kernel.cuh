@@ -75,6 +75,29 @@
 
 namespace dsaidx {
 
+// Phase stamps (a diagnostic build only, -DDSAIDX_PHASE_STAMPS): %globaltimer
+// at the phase boundaries of the first kPhaseUnits units of every CTA, read
+// back by idx_phase_stamps (decode.cu) and printed by the package's phases
+// module.  Slots: 0 kernel entry, 1 set-up done, 2 unit located, 3 query rows
+// landed, 4 B tile complete, 5 first key tile landed, 6 stream done,
+// 7 window sent, 8 windows received, 9 boundary known, 10 pool complete,
+// 11 ranks written, 12 unit end, 13 loop done, 14 exit.
+constexpr int kPhaseCtas = 2048;
+constexpr int kPhaseUnits = 4;
+constexpr int kPhaseSlots = 16;
+#ifdef DSAIDX_PHASE_STAMPS
+__device__ unsigned long long g_phase[kPhaseCtas][kPhaseUnits][kPhaseSlots];
+#define DSAIDX_PHASE(it, slot)                                                   \
+    do {                                                                         \
+        if ((it) < kPhaseUnits && blockIdx.x < kPhaseCtas)                       \
+            g_phase[blockIdx.x][(it)][(slot)] = global_timer_ns();               \
+    } while (0)
+#else
+#define DSAIDX_PHASE(it, slot) \
+    do {                       \
+    } while (0)
+#endif
+
 struct DecShared {
     uint32_t tmem_base;
     int abort;              // a pipeline wait of this CTA gave up (sticky)
@@ -141,6 +164,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
     const int tid = threadIdx.x;
     const int warp = warp_id(), lane = lane_id();
     const uint32_t rank = cluster_rank();
+    if (tid == 0) DSAIDX_PHASE(0, 0);
     const int cl = static_cast<int>(blockIdx.x) / kDecCl;
     const int ncl = static_cast<int>(gridDim.x) / kDecCl;
     int32_t* status = p.status;
@@ -214,6 +238,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
     cluster_wait();
     // the first half of the per-unit barrier (its wait follows the stream)
     cluster_arrive();
+    if (tid == 0) DSAIDX_PHASE(0, 1);
 
     uint32_t tcnt = 0;   // tiles streamed by this CTA so far (stage, phase and accumulator)
     uint32_t qcnt = 0;   // query loads (qbar / qready phases)
@@ -246,6 +271,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
         if (tid == 0) mbar_arrive_expect_tx(&ubar[(it + 1) & 1u], 4u);   // the next unit's id
         __syncthreads();
         const int b = ks->ub, seg = ks->useg, S = ks->uS;
+        if (tid == 0) DSAIDX_PHASE(it, 2);
         const bool valid = S >= 0 && S <= p.max_seq_len;
         const bool live = valid && S > 0;
         const int chunk = live ? dec_chunk(S) : kTileKeys;
@@ -341,6 +367,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                             const int a = static_cast<int>(T & 1u);
                             const uint32_t aph = (T >> 1) & 1u;
                             if (!mbar_wait(&full[s], ph, status, &ks->abort, wlim)) break;
+                            if (t == 0) DSAIDX_PHASE(it, 5);
                             if (T >= 2 && !mbar_wait(&tempty[a], aph ^ 1u, status, &ks->abort, wlim)) break;
                             tc_fence_after();
                             const uint32_t a_base = smem_u32(a_tiles + s * plan.a_stage_bytes);
@@ -370,6 +397,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                 if (warp < 6) {
                     if (tid == 64) mbar_arrive_expect_tx(qready, (kDecCl - 1) * kQPushBytes);
                     const bool have = __all_sync(0xffffffffu, mbar_wait(qbar, qcnt & 1u, status, &ks->abort, wlim));
+                    if (tid == 64) DSAIDX_PHASE(it, 3);
                     const int rl = (tid - 64) >> 4, part = tid & 15;
                     const int r = static_cast<int>(rank) * kQRows + rl;
                     if (have) {
@@ -406,6 +434,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                     const uint32_t lane_base = tmem + (static_cast<uint32_t>(qd * 32) << 16);
                     // every CTA's w' has arrived (the MMA waits on the same phase)
                     const bool qok = __all_sync(0xffffffffu, mbar_wait(qready, qcnt & 1u, status, &ks->abort, wlim));
+                    if (tid == 128) DSAIDX_PHASE(it, 4);
                     unsigned long long wr[32];
                     const unsigned long long* wq2 = reinterpret_cast<const unsigned long long*>(wq);
 #pragma unroll
@@ -465,6 +494,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
                     if (lane == 0) ks->emax[warp - 4] = kmax;
+                    if (tid == 128) DSAIDX_PHASE(it, 6);
                 }
             }
             ++qcnt;
@@ -541,7 +571,9 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                     dsmem_st_async_v4(dsmem_addr(mywin, dst) + 16u * c, v, dsmem_addr(wbar, dst));
                 }
             }
+            if (tid == 0) DSAIDX_PHASE(it, 7);
             const bool wok = __syncthreads_and(mbar_wait_cluster(wbar, scnt & 1u, status, 2 * kWaitLimitNs));
+            if (tid == 0) DSAIDX_PHASE(it, 8);
             ++scnt;
             // ------------------------------------ 2. boundary bin, counts, offsets
             // (the same decision in every CTA: a CTA failed a check or gave up a wait)
@@ -586,6 +618,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
             if (after < kk && kk <= after + hsum) ks->sel.bnd.bin = bt;
             __syncthreads();
             const int bstar = ks->sel.bnd.bin;
+            if (tid == 0) DSAIDX_PHASE(it, 9);
             // every CTA's count of scores in bins at or above the boundary: the
             // sum over the bins from it up (a CTA with scores below its window
             // and the boundary below that window: not known, the slow path)
@@ -699,6 +732,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                     }
                 }
                 const bool lok = __syncthreads_and(mbar_wait_cluster(lbar, lcnt & 1u, status, 2 * kWaitLimitNs));
+                if (tid == 0) DSAIDX_PHASE(it, 10);
                 ++lcnt;
                 if (lok) {
                     // ------------------------------------ 4. this CTA's eighth of the
@@ -714,6 +748,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                         rank_pool(pool, lo, hi, nsel, bstar - wlo, wlo, bstart, blen, scnt, scur, clist, srt,
                                   &ks->nmine, ks->sel.wcnt, emit);
                     }
+                    if (tid == 0) DSAIDX_PHASE(it, 11);
                     if (!single && rank == lead) {
                         // the run's entries per bin: every entry of a bin above the
                         // boundary, the boundary bin's first nsel - start
@@ -812,6 +847,7 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
         // into them; this CTA is done with its receive areas
         fence_proxy_async_smem();
         __syncthreads();
+        if (tid == 0) DSAIDX_PHASE(it, 12);
         cluster_arrive();
         // the next unit (drawn by rank 0 during this one); slot (it + 1) & 1 is
         // used every other unit, so this is its (it >> 1)-th use
@@ -821,12 +857,14 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
         __syncthreads();
     }
 
+    if (tid == 0) DSAIDX_PHASE(0, 13);
     // no CTA leaves while another may still send it something
     cluster_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, 2 * kN);
+    if (tid == 32) DSAIDX_PHASE(0, 14);
 }
 
 }  // namespace dsaidx
