@@ -254,3 +254,21 @@ def test_slot_output_is_the_block_table_translate(mode):
         for b in range(B):
             assert np.array_equal(slots[b], oracle.translate_slots(W.block_table[b], bs, idx[b]))
         assert np.all(slots[2] == -1)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_large_batch_many_units_per_cluster(mode):
+    # 300 sequences (more than one per scanning thread), random lengths with
+    # empty ones and two multi-segment ones: each cluster takes about nine
+    # units from the counter, alternating the next-unit barrier slots
+    rng = np.random.default_rng(131 + mode)
+    lens = rng.integers(0, 5000, 300)
+    lens[::37] = 0
+    lens[5], lens[200] = 70000, 131073
+    W = wl.make_workload("many", [int(x) for x in lens], [1] * 300, topk=256, seed=133 + mode)
+    got = run_decode(W, mode)
+    rows = [b for b in range(W.batch) if W.seq_lens[b] > 0]
+    check(W, mode, got, rows=rows)
+    for b in range(W.batch):
+        if W.seq_lens[b] == 0:
+            assert np.all(got["idx"][b] == -1)
