@@ -75,13 +75,17 @@ cudaError_t launch_decode_t(const idx_cache* c, const ScoreParams& p, int64_t un
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(plan.total);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kDecCl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // the set-up may overlap the previous kernel (the kernel waits for it,
+    // griddepcontrol.wait, before it reads anything that kernel writes)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     kt_mark(st);
     e = cudaLaunchKernelEx(&cfg, kern, c->tmap, p);
     kt_mark(st);

@@ -240,6 +240,11 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
     cluster_arrive();
     if (tid == 0) DSAIDX_PHASE(0, 1);
 
+    // Launched with programmatic serialization, the set-up above may overlap
+    // the previous kernel in the stream (the key store); nothing below runs
+    // before that grid has finished and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     uint32_t tcnt = 0;   // tiles streamed by this CTA so far (stage, phase and accumulator)
     uint32_t qcnt = 0;   // query loads (qbar / qready phases)
     uint32_t scnt = 0;   // window exchanges (wbar phases)

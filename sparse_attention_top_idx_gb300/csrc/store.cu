@@ -82,6 +82,10 @@ __global__ void __launch_bounds__(256) store_keys_kernel(const uint4* __restrict
     const unsigned hmask = 0xFFFFu << (threadIdx.x & 16);  // this half-warp's lanes
     const int64_t tok0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
     const int64_t tstride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
+    // A kernel launched after this one with programmatic serialization (the
+    // decode kernel) may start its set-up now; it waits for this grid's
+    // writes before it reads any key.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // The trip count is uniform over a half-warp, which is all the shuffles span.
     for (int64_t tok = tok0; tok < n; tok += tstride) {
         const int64_t slot = slots[tok];
