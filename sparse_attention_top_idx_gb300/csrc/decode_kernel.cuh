@@ -165,6 +165,10 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
     const int warp = warp_id(), lane = lane_id();
     const uint32_t rank = cluster_rank();
     if (tid == 0) DSAIDX_PHASE(0, 0);
+    // a kernel launched next with programmatic serialization (the next key
+    // store) may be scheduled now; it waits for this grid to finish before it
+    // touches anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int cl = static_cast<int>(blockIdx.x) / kDecCl;
     const int ncl = static_cast<int>(gridDim.x) / kDecCl;
     int32_t* status = p.status;

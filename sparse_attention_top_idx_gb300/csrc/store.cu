@@ -84,8 +84,11 @@ __global__ void __launch_bounds__(256) store_keys_kernel(const uint4* __restrict
     const int64_t tstride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
     // A kernel launched after this one with programmatic serialization (the
     // decode kernel) may start its set-up now; it waits for this grid's
-    // writes before it reads any key.
+    // writes before it reads any key.  This grid, launched the same way, waits
+    // for the previous grid in the stream (a decode reading the pool) before
+    // it reads its inputs or writes a key.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // The trip count is uniform over a half-warp, which is all the shuffles span.
     for (int64_t tok = tok0; tok < n; tok += tstride) {
         const int64_t slot = slots[tok];
@@ -163,9 +166,19 @@ cudaError_t launch_store(const idx_cache* c, const void* k, const int64_t* slots
     const bool fp8 = c->key_dtype == IDX_KEY_FP8_E4M3;
     auto kern = fp8 ? (rotate ? store_keys_kernel<true, true> : store_keys_kernel<true, false>)
                     : (rotate ? store_keys_kernel<false, true> : store_keys_kernel<false, false>);
-    kern<<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<const uint4*>(k), slots, n, c->pool,
-                                                   c->num_blocks, c->block_size, c->block_bytes, status, rs);
-    return cudaGetLastError();
+    // programmatic serialization: the launch may overlap the previous kernel,
+    // which the kernel waits for (griddepcontrol.wait) before any access
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint4*>(k), slots, n, c->pool, c->num_blocks,
+                              c->block_size, c->block_bytes, status, rs);
 }
 
 }  // namespace dsaidx
