@@ -42,20 +42,45 @@ N_POOL_COPIES = 9
 
 # DRAM bytes per launch of the dominant kernels from ncu captures
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
-# hash of the kernel sources they were taken on; a stale hash reports null.
+# hash of the measured kernel's sources (its translation unit and every header
+# it includes) when they were taken; a stale hash reports null.
 NCU_TRAFFIC = {
-    ("decode", "50fe28e59007d687"): 31443968 + 0,
-    ("longctx", "50fe28e59007d687"): 277238272 + 2797312,
-    ("prefill", "50fe28e59007d687"): 139622144 + 531330560,   # the scoring kernel
+    ("decode", "b1064f746bcec8b2"): 31446272 + 0,
+    ("longctx", "b1064f746bcec8b2"): 277238272 + 2780160,
+    ("prefill", "53c45c72bce93128"): 139622144 + 531330560,   # the scoring kernel
 }
+KERNEL_TU = {"decode": "decode.cu", "longctx": "decode.cu", "prefill": "prefill.cu"}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(tu: str) -> str:
+    """sha256 (first 16 hex digits) of a kernel translation unit and the
+    closure of the quoted headers it includes (csrc/ and include/)."""
+    dirs = [os.path.join(ROOT, "sparse_attention_top_idx_gb300", "csrc"), os.path.join(ROOT, "include")]
+    seen, todo = [], [tu]
+    while todo:
+        name = todo.pop()
+        if name in seen:
+            continue
+        path = next((os.path.join(d, name) for d in dirs if os.path.exists(os.path.join(d, name))), None)
+        if path is None:
+            continue
+        seen.append(name)
+        with open(path) as f:
+            for line in f:
+                t = line.strip()
+                if t.startswith("#include \""):
+                    todo.append(t.split('"')[1])
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "sparse_attention_top_idx_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in sorted(seen):
+        path = next(os.path.join(d, name) for d in dirs if os.path.exists(os.path.join(d, name)))
+        h.update(name.encode())
+        with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def traffic_of(workload: str):
+    return NCU_TRAFFIC.get((workload, kernel_source_hash(KERNEL_TU[workload])))
 
 
 def measured_peaks():
@@ -406,14 +431,14 @@ def roofline_hbm(algo_bytes, kern_ms, peak_gbs, traffic):
             "kernel_us": round(avg_ms * 1e3, 3), "algorithmic_bytes": int(algo_bytes)}
 
 
-def bench_long_context(device, steps, warmup, peaks, src_hash):
+def bench_long_context(device, steps, warmup, peaks):
     import torch
     from sparse_attention_top_idx_gb300 import workloads as wl
     W = wl.long_context()
     b = DecodeBench(W, device, copies=2)     # 277 MB per copy: larger than L2
     total_ms, kern_ms, g = time_steps(b, steps, warmup, None, device)
     del g
-    tr = NCU_TRAFFIC.get(("longctx", src_hash))
+    tr = traffic_of("longctx")
     out = {"workload": W.name, "keys_per_step": b.keys, "ms_per_step": round(total_ms / steps, 5),
            "value": round(b.keys / (total_ms / steps * 1e-3), 1), "unit": UNIT,
            "roofline": roofline_hbm(b.algo_bytes(), kern_ms, peaks["hbm_gbs"], tr)}
@@ -458,7 +483,7 @@ def tensor_peaks():
     return res
 
 
-def bench_prefill(device, steps, warmup, peaks, src_hash):
+def bench_prefill(device, steps, warmup, peaks):
     import torch
     from sparse_attention_top_idx_gb300 import dsaidx
     from sparse_attention_top_idx_gb300 import workloads as wl
@@ -500,7 +525,7 @@ def bench_prefill(device, steps, warmup, peaks, src_hash):
            "kernels_us": {"score": round(score_ms * 1e3, 1), "select": round(select_ms * 1e3, 1)},
            "roofline": {"bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_peak, 1),
                         "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4),
-                        "traffic": NCU_TRAFFIC.get(("prefill", src_hash)),
+                        "traffic": traffic_of("prefill"),
                         "kernel_us": round(score_ms * 1e3, 1),
                         "algorithmic_flop": flops,
                         "whole_call_frac": round(flops / (ms * 1e-3) / 1e12 / fp8_peak, 4),
@@ -685,12 +710,11 @@ def main():
     from sparse_attention_top_idx_gb300 import dsaidx, workloads as wl
     dsaidx.load()
     peaks = measured_peaks()
-    src_hash = kernel_source_hash()
     if args.only == "longctx":
-        print(json.dumps(bench_long_context(device, args.steps, args.warmup, peaks, src_hash)))
+        print(json.dumps(bench_long_context(device, args.steps, args.warmup, peaks)))
         return 0
     if args.only == "prefill":
-        print(json.dumps(bench_prefill(device, args.steps, args.warmup, peaks, src_hash)))
+        print(json.dumps(bench_prefill(device, args.steps, args.warmup, peaks)))
         return 0
 
     W = wl.decode_batch()
@@ -710,7 +734,7 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms, dist, device)
     e2e_eager_ms = max_over_ranks(e2e_eager_ms, dist, device)
 
-    tr = NCU_TRAFFIC.get(("decode", src_hash))
+    tr = traffic_of("decode")
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
             "us_per_step": round(ms_step * 1e3, 2), "higher_is_better": True, "scaling": "weak",
@@ -738,8 +762,8 @@ def main():
     del bench
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_extra:
-        line["long_context"] = bench_long_context(device, max(10, args.steps // 4), args.warmup, peaks, src_hash)
-        line["prefill"] = bench_prefill(device, max(3, args.steps // 40), 3, peaks, src_hash)
+        line["long_context"] = bench_long_context(device, max(10, args.steps // 4), args.warmup, peaks)
+        line["prefill"] = bench_prefill(device, max(3, args.steps // 40), 3, peaks)
     if rank == 0 and not args.no_extra:
         line["precision"] = bench_precision(device)
     if rank == 0 and not args.no_cpu:
