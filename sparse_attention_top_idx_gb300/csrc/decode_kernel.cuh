@@ -68,6 +68,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "headsum.cuh"
 #include "internal.h"
 #include "qprep.cuh"
 #include "segsel.cuh"
@@ -439,15 +440,13 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                     // block ids in place, histogram cleared
                     asm volatile("bar.sync 2, %0;" ::"r"(32 + 32 * kEpiWarps) : "memory");
                     const int qd = warp & 3;
-                    const int row = qd * 32 + lane;
+                    const int row = qd * 32 + head_sum_row(lane);   // the row this lane scores
                     const uint32_t lane_base = tmem + (static_cast<uint32_t>(qd * 32) << 16);
                     // every CTA's w' has arrived (the MMA waits on the same phase)
                     const bool qok = __all_sync(0xffffffffu, mbar_wait(qready, qcnt & 1u, status, &ks->abort, wlim));
                     if (tid == 128) DSAIDX_PHASE(it, 4);
-                    unsigned long long wr[32];
-                    const unsigned long long* wq2 = reinterpret_cast<const unsigned long long*>(wq);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) wr[i] = wq2[i];
+                    unsigned long long wr[8];
+                    load_head_weights(wq, lane, wr);
                     // key scale of this thread's key in tile t (0 past the chunk or for a bad id)
                     auto scale_of = [&](int t) -> float {
                         if constexpr (!kFp8) {
@@ -473,24 +472,13 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                         // waits are combined over the warp so that every lane leaves together
                         if (!__all_sync(0xffffffffu, mbar_wait(&tfull[a], aph, status, &ks->abort, wlim))) break;
                         tc_fence_after();
-                        // sum_h w'[h] * max(D[h], 0) with max(D, 0) = (D + |D|) / 2, even and
-                        // odd heads in the two lanes of a packed pair, 16 heads per TMEM load
-                        unsigned long long acc = 0ull;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            float v[16];
-                            tmem_ld16(lane_base + static_cast<uint32_t>(a * kN + 16 * c), v);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                acc = f2_fma(wr[8 * c + i],
-                                             f2_pack(v[2 * i] + fabsf(v[2 * i]), v[2 * i + 1] + fabsf(v[2 * i + 1])),
-                                             acc);
-                        }
-                        const float2 pr = f2_unpack(acc);
-                        const float res = kscale * (0.5f * (pr.x + pr.y));
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&tempty[a]);
+                        // every TMEM read of the buffer has completed when release runs
+                        const float hs = head_sum_rows(lane_base + static_cast<uint32_t>(a * kN), wr, lane, [&] {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&tempty[a]);
+                        });
+                        const float res = kscale * (0.5f * hs);
                         const int i = t * kTileKeys + row;
                         if (i < nkeys) {
                             csc[i] = res;

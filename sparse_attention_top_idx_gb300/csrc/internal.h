@@ -133,8 +133,10 @@ static_assert(3 * 16384 >= 4096 * 4 + 4096 * 8, "the selection scratch fits the 
 constexpr int kDecMaxClusters(int sms) { return 2 * sms / kDecCl; }   // two CTAs per SM at most
 
 // Shared-memory plan of the prefill scoring kernel (kPrefillQT queries per
-// CTA): key stages, the B tile, key scales, head weights, the staged bf16
-// query rows, block ids, scratch and barriers.
+// CTA): key stages (seven of fp8 codes, two of bf16 keys; the epilogue reads
+// the fp8 key scales from the pool, so a stage holds codes only and is free
+// once the MMA has read it), the B tile, head weights, the staged bf16 query
+// rows, block ids, scratch and barriers (at most 8 stages).
 struct SmemPlan {
     int stages, a_stage_bytes, q_bytes, n_cols;
     int a_off, q_off, scale_off, w_off, raw_off, bid_off, misc_off, bar_off;
@@ -144,13 +146,13 @@ __host__ __device__ inline SmemPlan make_plan(bool fp8, int qt, int chunk) {
     (void)chunk;
     SmemPlan p{};
     p.n_cols = 64 * qt;
-    p.stages = fp8 ? 4 : 2;
+    p.stages = fp8 ? 7 : 2;
     p.a_stage_bytes = fp8 ? 16384 : 32768;
     p.q_bytes = p.n_cols * (fp8 ? 128 : 256);
     int o = 0;
     p.a_off = o;       o += p.stages * p.a_stage_bytes;
     p.q_off = o;       o += p.q_bytes;
-    p.scale_off = o;   o += fp8 ? p.stages * 512 : 0;
+    p.scale_off = o;   // no scale ring
     p.w_off = o;       o += p.n_cols * 4;
     p.raw_off = o;     o += qt * 16384;
     p.bid_off = o;     o += kBidWindow * 4;  // prefetched block ids

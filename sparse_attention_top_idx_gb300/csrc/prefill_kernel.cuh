@@ -21,15 +21,17 @@
 // Warp roles (640 threads): warp 0 lane 0 starts the query rows' bulk copy,
 // then the warp prefetches block ids and lane 0 issues the key TMA; warps
 // 1..19 quantise the queries into the B tile; warp 1 owns TMEM and its lane 0
-// issues the MMAs; warps 4..19 (one per TMEM lane quadrant and query, one key
-// row per thread) run the epilogue ks[s] * sum_h w'[t, h] * max(D, 0) with
-// the query's head weights held in registers and write the causally visible
-// scores to the workspace for the row select kernel.
+// issues the MMAs; warps 4..19 (one per TMEM lane quadrant and query; each
+// lane sums a quarter of the heads of four key rows, then the four lanes of
+// a row group combine theirs) run the epilogue ks[s] * sum_h w'[t, h] *
+// max(D, 0) with the head weights held in registers and write the causally
+// visible scores to the workspace for the row select kernel.
 #pragma once
 
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "headsum.cuh"
 #include "internal.h"
 #include "qprep.cuh"
 #include "topk.cuh"
@@ -51,11 +53,11 @@ __global__ void __maxnreg__(96)
     prefill_score_kernel(const __grid_constant__ CUtensorMap tmap, const ScoreParams p) {
     constexpr int kQT = kPrefillQT;
     constexpr int kBlock = kPrefillThreads;
-    constexpr int kEpiWarps = 16;                          // one per (TMEM lane quadrant, query)
+    constexpr int kEpiWarps = 16;                          // per (TMEM buffer, lane quadrant, query pair)
     constexpr int kN = 64 * kQT;
     constexpr int kBlocksPerTile = kTileKeys / kBs;
     constexpr int kKSteps = kFp8 ? 4 : 8;
-    constexpr uint32_t kBlockTx = kFp8 ? (kBs * 128 + kBs * 4) : (kBs * 256);
+    constexpr uint32_t kBlockTx = kFp8 ? (kBs * 128) : (kBs * 256);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -64,17 +66,16 @@ __global__ void __maxnreg__(96)
     const int kStages = plan.stages;
     uint8_t* a_tiles = smem + plan.a_off;
     uint8_t* qtile = smem + plan.q_off;
-    float* scales = reinterpret_cast<float*>(smem + plan.scale_off);
     float* wq = reinterpret_cast<float*>(smem + plan.w_off);
     uint8_t* raw = smem + plan.raw_off;                     // staged query rows (bf16)
     PrefillShared* ks = reinterpret_cast<PrefillShared*>(smem + plan.misc_off);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
     uint64_t* full = bars;                 // [stages] TMA -> MMA
-    uint64_t* empty = bars + 4;            // [stages] MMA (+ epilogue) -> TMA
-    uint64_t* tfull = bars + 8;            // [2] MMA -> epilogue
-    uint64_t* tempty = bars + 10;          // [2] epilogue -> MMA
-    uint64_t* mdone = bars + 12;           // MMA drain at exit
-    uint64_t* qbar = bars + 13;            // query rows staged
+    uint64_t* empty = bars + 8;            // [stages] MMA -> TMA
+    uint64_t* tfull = bars + 16;           // [2] MMA -> epilogue
+    uint64_t* tempty = bars + 18;          // [2] epilogue -> MMA
+    uint64_t* mdone = bars + 20;           // MMA drain at exit
+    uint64_t* qbar = bars + 21;            // query rows staged
 
     const int tid = threadIdx.x;
     const int warp = warp_id(), lane = lane_id();
@@ -164,11 +165,11 @@ __global__ void __maxnreg__(96)
         } else if (lane == 1) {
             for (int s = 0; s < kStages; ++s) {
                 mbar_init(&full[s], 1);
-                mbar_init(&empty[s], kFp8 ? 1 + kEpiWarps : 1);
+                mbar_init(&empty[s], 1);
             }
             for (int a = 0; a < 2; ++a) {
                 mbar_init(&tfull[a], 1);
-                mbar_init(&tempty[a], kEpiWarps);
+                mbar_init(&tempty[a], kEpiWarps / 2);
             }
             mbar_init(mdone, 1);
             fence_mbar_init();
@@ -241,9 +242,6 @@ __global__ void __maxnreg__(96)
                         if (phys[j] < 0) continue;
                         if constexpr (kFp8) {
                             tma_load_3d(a_s + j * kBs * 128, &tmap, &full[s], 0, 0, phys[j], pol);
-                            bulk_load(scales + s * 128 + j * kBs,
-                                      p.pool + static_cast<int64_t>(phys[j]) * p.block_bytes + kBs * 128,
-                                      kBs * 4, &full[s], pol);
                         } else {
                             tma_load_3d(a_s + j * kBs * 128, &tmap, &full[s], 0, 0, phys[j], pol);
                             tma_load_3d(a_s + 16384 + j * kBs * 128, &tmap, &full[s], 64, 0, phys[j], pol);
@@ -302,62 +300,62 @@ __global__ void __maxnreg__(96)
         mma_commit(mdone);
         mbar_wait(mdone, 0, status, nullptr);
     } else if (warp >= 4) {
-        // epilogue: one key row per thread; warp w reads TMEM lane quadrant
-        // w % 4 for query j0 = (w - 4) / 4 of the group
+        // epilogue: two groups of 8 warps, group g taking the tiles of TMEM
+        // buffer g (tiles t = g, g + 2, ...), so that one group works while
+        // the other waits for its next accumulator.  Epilogue warp e = w - 4
+        // reads TMEM lane quadrant qd = w % 4 (32 keys) for queries
+        // 2 (e / 8) and 2 (e / 8) + 1 of the group; each lane keeps the
+        // weights of its 16 heads of both queries in registers and writes the
+        // scores of quadrant row head_sum_row(lane).
+        const int e = warp - 4;
         const int qd = warp & 3;
-        const int row = qd * 32 + lane;
-        const int j0 = (warp - 4) >> 2;
+        const int g = (e >> 2) & 1;
+        const int jq = 2 * (e >> 3);
+        const int orow = qd * 32 + head_sum_row(lane);
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(qd * 32) << 16);
-        // the query's 64 head weights stay in registers for the whole loop,
-        // and TMEM is read 16 columns at a time to make room.  (Reloading
-        // them per tile made the shared-memory load pipe the kernel's limit:
-        // a broadcast load fills the 32 lanes' registers at 128 bytes per
-        // wavefront, 64 wavefronts per warp-tile.)
-        unsigned long long wr[32];
-        const unsigned long long* wq2 = reinterpret_cast<const unsigned long long*>(wq + j0 * 64);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) wr[i] = wq2[i];
-        const int vis_pos = j0 < ks->nrows ? ks->pos[j0] : -1;
-        const int64_t out_row = static_cast<int64_t>(ks->row0 + j0) * p.score_stride;
-        for (int t = 0; t < ntiles; ++t) {
-            const int s = t % kStages;
-            const uint32_t ph = static_cast<uint32_t>(t / kStages) & 1u;
-            const int a = t & 1;
+        unsigned long long wr0[8];
+        load_head_weights(wq + jq * 64, lane, wr0);
+        const int vis0 = jq < ks->nrows ? ks->pos[jq] : -1;
+        const int vis1 = jq + 1 < ks->nrows ? ks->pos[jq + 1] : -1;
+        float* out0 = p.scores + static_cast<int64_t>(ks->row0 + jq) * p.score_stride;
+        float* out1 = out0 + p.score_stride;
+        // key scale of this lane's key in tile t, read from the pool (0 past
+        // the keys or for a bad block id, whose rows are flagged anyway)
+        const int* bt_row = p.block_table + static_cast<int64_t>(seq_b) * p.mbps;
+        auto scale_of = [&](int t) -> float {
+            if constexpr (!kFp8) {
+                return 1.0f;
+            } else {
+                const int key = key_begin + t * kTileKeys + orow;
+                if (t >= ntiles || key >= key_end || key / kBs >= p.mbps) return 0.0f;
+                const int pb = __ldg(bt_row + key / kBs);
+                if (pb < 0 || pb >= p.num_blocks) return 0.0f;
+                return __ldg(reinterpret_cast<const float*>(p.pool + static_cast<int64_t>(pb) * p.block_bytes +
+                                                            kBs * 128) + (key % kBs));
+            }
+        };
+        float sc0 = scale_of(g), sc1 = scale_of(g + 2);
+        for (int t = g; t < ntiles; t += 2) {
             const uint32_t aph = static_cast<uint32_t>(t >> 1) & 1u;
+            const float kscale = sc0;
+            sc0 = sc1;
+            sc1 = scale_of(t + 4);
             // waits are combined over the warp so that every lane leaves together
-            if (!__all_sync(0xffffffffu, mbar_wait(&tfull[a], aph, status, &ks->abort, p.wait_ns))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&tfull[g], aph, status, &ks->abort, p.wait_ns))) break;
             tc_fence_after();
-            float kscale = 1.0f;
-            if constexpr (kFp8) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, status, &ks->abort, p.wait_ns))) break;
-                kscale = scales[s * 128 + row];
+            const uint32_t col = lane_base + static_cast<uint32_t>(g * kN + jq * 64);
+            const float h0 = head_sum_rows(col, wr0, lane, [] {});
+            // every TMEM read of the buffer by this warp has completed when release runs
+            unsigned long long wr1[8];
+            load_head_weights(wq + (jq + 1) * 64, lane, wr1);
+            const float h1 = head_sum_rows(col + 64, wr1, lane, [&] {
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-            }
-            // sum_h w'[h] * max(D[h], 0): max(D, 0) as D + |D| = 2 max(D, 0)
-            // exactly, an add with an absolute-value operand on the FMA pipe
-            // (the ALU pipe, where a max goes, was the epilogue's busiest;
-            // moving all 64 there measured fastest, and one accumulator chain
-            // faster than two), even and odd heads in the two lanes of a
-            // packed pair, the factor 2 removed at the end (exact); 16 heads
-            // per TMEM load
-            unsigned long long acc = 0ull;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v[16];
-                tmem_ld16(lane_base + static_cast<uint32_t>(a * kN + j0 * 64 + 16 * c), v);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    acc = f2_fma(wr[8 * c + i],
-                                 f2_pack(v[2 * i] + fabsf(v[2 * i]), v[2 * i + 1] + fabsf(v[2 * i + 1])), acc);
-            }
-            const float2 pr = f2_unpack(acc);
-            const float res = kscale * (0.5f * (pr.x + pr.y));
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[a]);
-            const int key = key_begin + t * kTileKeys + row;
-            if (key <= vis_pos) p.scores[out_row + key] = res;
+                if (lane == 0) mbar_arrive(&tempty[g]);
+            });
+            const int key = key_begin + t * kTileKeys + orow;
+            if (key <= vis0) out0[key] = kscale * (0.5f * h0);
+            if (key <= vis1) out1[key] = kscale * (0.5f * h1);
         }
     }
     tc_fence_before();
