@@ -86,6 +86,8 @@ class Oracle:
         L.orc_store_keys_any.argtypes = [P, I64, I, I, I, P, P, I64, I]
         L.orc_store_keys_any.restype = I64
         L.orc_wht_rows.argtypes = [P, I64, I, P]
+        L.orc_e2m1_encode_n.argtypes = [P, P, I64]
+        L.orc_fp4_roundtrip_rows.argtypes = [P, I64, I, P]
         L.orc_quant_rows_f32.argtypes = [P, I64, I, P, P]
         L.orc_f32_to_bf16_n.argtypes = [P, P, I64]
         L.orc_translate_slots.argtypes = [P, I64, I, P, I64, P]
@@ -165,7 +167,37 @@ class Oracle:
     def rotated_key_rows(self, x_bf16, dtype: int):
         """What the rotated store keeps for bf16 key rows: fp8 (codes, scales)
         of the rotated floats, or their bf16 bits rounded to nearest even."""
-        y = self.wht_rows(x_bf16)
+        return self.stored_key_rows(x_bf16, dtype, rotate=True)
+
+
+    def e2m1_encode(self, x) -> np.ndarray:
+        """fp32 -> e2m1 codes (sign << 3 | code), nearest, ties to the even code."""
+        x = _c(x, np.float32)
+        out = np.empty(x.shape, np.uint8)
+        self.L.orc_e2m1_encode_n(_p(x), _p(out), x.size)
+        return out
+
+
+    def fp4_roundtrip_rows(self, x) -> np.ndarray:
+        """The fp4 round trip of float rows [R, d] (d a multiple of 32): per
+        block of 32 the scale amax / 6, e2m1 codes, decoded back to float."""
+        x = _c(x, np.float32)
+        R, d = x.shape
+        y = np.empty((R, d), np.float32)
+        self.L.orc_fp4_roundtrip_rows(_p(x), R, d, _p(y))
+        return y
+
+
+    def stored_key_rows(self, x_bf16, dtype: int, rotate: bool = False, fp4: bool = False):
+        """What the store keeps for bf16 key rows with the given options: fp8
+        (codes, scales) or bf16 bits.  rotate: Walsh-Hadamard first; fp4: then
+        the fp4 round trip; the float result is quantised or rounded."""
+        x = _c(x_bf16, np.uint16)
+        if not rotate and not fp4:
+            return self.quantize_rows(x) if dtype == FP8 else x.copy()
+        y = self.wht_rows(x) if rotate else (x.astype(np.uint32) << 16).view(np.float32)
+        if fp4:
+            y = self.fp4_roundtrip_rows(y)
         if dtype == FP8:
             return self.quantize_rows_f32(y)
         return self.f32_to_bf16(y)
@@ -188,16 +220,18 @@ class Oracle:
 
 
     def store_keys(self, pool: np.ndarray, k_bf16, slot_mapping, bs: int, dtype: int,
-                   rotate: bool = False) -> int:
+                   rotate: bool = False, fp4: bool = False) -> int:
         """Write keys into a flat uint8 pool in place (Walsh-Hadamard rotated
-        first when rotate); returns tokens written."""
+        first when rotate, then the fp4 round trip when fp4); returns tokens
+        written."""
         assert pool.dtype == np.uint8 and pool.flags.c_contiguous
         k = _c(k_bf16, np.uint16)
         sm = _c(slot_mapping, np.int64)
         n, d = k.shape
         bb = self.block_bytes(dtype, bs, d)
         nb = pool.size // bb
-        r = self.L.orc_store_keys_any(_p(pool), nb, bs, d, dtype, _p(k), _p(sm), n, 1 if rotate else 0)
+        r = self.L.orc_store_keys_any(_p(pool), nb, bs, d, dtype, _p(k), _p(sm), n,
+                                      (1 if rotate else 0) | (2 if fp4 else 0))
         if r < 0:
             raise ValueError("slot out of range")
         return int(r)

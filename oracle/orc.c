@@ -31,7 +31,10 @@
  * all-zero codes; the query is quantised the same way per (t, h) row and its
  * scale sq is folded into the head weight, w' = fl32(w * sq); a query at
  * position pos sees keys s <= pos; ties in score go to the lower index; the
- * top-k is listed in descending score order and padded with -1.
+ * top-k is listed in descending score order and padded with -1.  The fp4
+ * round trip (below) keeps fl32(amax / 6) per block of 32 as the scale, rounds
+ * fl32(x / scale) to the nearest e2m1 value (ties to the even code,
+ * saturating at 6) and hands on fl32(code * scale) in fp32.
  *
  * Build: cc -O2 -ffp-contract=off -fPIC -shared [-fopenmp] orc.c -o liborc.so
  * (-ffp-contract=off keeps every multiply and add separately rounded, so x86
@@ -273,6 +276,98 @@ void orc_quant_rows(const uint16_t* x_bf16, int64_t rows, int d, uint8_t* codes,
 }
 
 /* ------------------------------------------------------------------------ */
+/* fp4 (e2m1) round trip of an index key in blocks of 32                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The 4-bit float e2m1 (1 sign, 2 exponent and 1 mantissa bit, no infinities
+ * or NaN): code c = 0..7 has magnitude orc_e2m1_mag[c] (0 and 0.5 are the
+ * zero and the subnormal, then 1, 1.5, 2, 3, 4, 6), bit 3 is the sign.
+ */
+static const double orc_e2m1_mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/*
+ * Encode a finite fp32 value to e2m1: the code whose magnitude is nearest to
+ * |x| (found by trying all eight), a tie between two neighbours going to the
+ * even code (low bit 0); magnitudes from 6 up saturate to 6 (taken before the
+ * search: far above 6 the double distances to 4 and 6 round to one value).
+ * The sign bit is kept, so -0 and negative values that round to zero give 0x8.
+ */
+uint8_t orc_e2m1_encode(float x)
+{
+    double a = fabs((double)x);
+    int c, best = 0;
+    double bd = a;
+    if (a >= orc_e2m1_mag[7])
+        return (uint8_t)((signbit(x) ? 8 : 0) | 7);
+    for (c = 1; c < 8; c++) {
+        double dist = fabs(a - orc_e2m1_mag[c]);
+        if (dist < bd || (dist == bd && (c & 1) == 0)) {
+            best = c;
+            bd = dist;
+        }
+    }
+    return (uint8_t)((signbit(x) ? 8 : 0) | best);
+}
+
+double orc_e2m1_decode(uint8_t c)
+{
+    double m = orc_e2m1_mag[c & 7];
+    return (c & 8) ? -m : m;
+}
+
+void orc_e2m1_encode_n(const float* x, uint8_t* out, int64_t n)
+{
+    int64_t i;
+    for (i = 0; i < n; i++)
+        out[i] = orc_e2m1_encode(x[i]);
+}
+
+/*
+ * The fp4 round trip that "DeepSeek-V4 index_topk=1024 sparse indexer can't
+ * recall verbatim lines" (ROCm/ATOM issue #1507), section "Where (main
+ * 0c7d50f9)", lists on the indexer's key path after the rotation
+ * (fp4_act_quant_inplace(kv, 32), the fp4 quantisation-aware round trip):
+ * every block of ORC_FP4_BLOCK = 32 consecutive values gets its own scale
+ * s = fl32(amax / 6) (6 is the largest e2m1 magnitude),
+ * each value x becomes the e2m1 code of fl32(x / s) and is replaced by
+ * fl32(code * s), the decoded value.  A block whose values are all zero keeps
+ * them.  d must be a multiple of 32; the output stays in fp32.
+ */
+#define ORC_FP4_BLOCK 32
+
+void orc_fp4_roundtrip_row(const float* x, int d, float* y)
+{
+    int b, j;
+    for (b = 0; b < d; b += ORC_FP4_BLOCK) {
+        float amax = 0.0f, s;
+        for (j = 0; j < ORC_FP4_BLOCK; j++) {
+            float a = fabsf(x[b + j]);
+            if (a > amax)
+                amax = a;
+        }
+        if (amax == 0.0f) {
+            for (j = 0; j < ORC_FP4_BLOCK; j++)
+                y[b + j] = x[b + j];
+            continue;
+        }
+        s = amax / 6.0f;
+        for (j = 0; j < ORC_FP4_BLOCK; j++) {
+            float v = x[b + j] / s;
+            y[b + j] = (float)(orc_e2m1_decode(orc_e2m1_encode(v)) * (double)s);
+        }
+    }
+}
+
+void orc_fp4_roundtrip_rows(const float* x, int64_t rows, int d, float* y)
+{
+    int64_t r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; r++)
+        orc_fp4_roundtrip_row(x + r * d, d, y + r * d);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Paged index-key cache                                                     */
 /* ------------------------------------------------------------------------ */
 
@@ -293,19 +388,22 @@ int64_t orc_block_bytes(int dtype, int bs, int d)
 
 /*
  * Write n keys into the pool: token i goes to slot slot_mapping[i] =
- * block * bs + offset; a negative slot is skipped.  With rotate != 0 each key
- * is first Walsh-Hadamard rotated (orc_wht_row) and the float result is what
- * is quantised (fp8) or rounded to bf16.  Returns the number of tokens
- * written, or -1 if a slot is out of range (-2 for d > ORC_MAX_D).
+ * block * bs + offset; a negative slot is skipped.  mode bit 0 (rotate): each
+ * key is first Walsh-Hadamard rotated (orc_wht_row); mode bit 1 (fp4): the
+ * float row then takes the fp4 round trip (orc_fp4_roundtrip_row).  With
+ * either, the float result is what is quantised (fp8) or rounded to bf16.
+ * Returns the number of tokens written, or -1 if a slot is out of range (-2
+ * for d > ORC_MAX_D or, with fp4, d not a multiple of 32).
  */
 int64_t orc_store_keys_any(uint8_t* pool, int64_t num_blocks, int bs, int d, int dtype,
-                           const uint16_t* k_bf16, const int64_t* slot_mapping, int64_t n, int rotate)
+                           const uint16_t* k_bf16, const int64_t* slot_mapping, int64_t n, int mode)
 {
     int64_t i, written = 0;
     int64_t bb = orc_block_bytes(dtype, bs, d);
-    float y[ORC_MAX_D];
+    float y[ORC_MAX_D], t[ORC_MAX_D];
     int j;
-    if (d > ORC_MAX_D)
+    const int rotate = mode & 1, fp4 = (mode >> 1) & 1, fl = rotate || fp4;
+    if (d > ORC_MAX_D || (fp4 && d % ORC_FP4_BLOCK != 0))
         return -2;
     for (i = 0; i < n; i++) {
         int64_t slot = slot_mapping[i];
@@ -320,14 +418,21 @@ int64_t orc_store_keys_any(uint8_t* pool, int64_t num_blocks, int bs, int d, int
         base = pool + blk * bb;
         if (rotate)
             orc_wht_row(k_bf16 + i * d, d, y);
+        else if (fp4)
+            for (j = 0; j < d; j++)
+                y[j] = orc_bf16_to_f32(k_bf16[i * d + j]);
+        if (fp4) {
+            orc_fp4_roundtrip_row(y, d, t);
+            memcpy(y, t, (size_t)d * sizeof(float));
+        }
         if (dtype == ORC_FP8) {
             float sc;
-            if (rotate)
+            if (fl)
                 orc_quant_row_f32(y, d, base + off * d, &sc);
             else
                 orc_quant_row(k_bf16 + i * d, d, base + off * d, &sc);
             memcpy(base + (int64_t)bs * d + off * 4, &sc, 4);
-        } else if (rotate) {
+        } else if (fl) {
             for (j = 0; j < d; j++) {
                 uint16_t b = orc_f32_to_bf16(y[j]);
                 memcpy(base + off * d * 2 + (int64_t)j * 2, &b, 2);

@@ -15,6 +15,7 @@ import torch
 
 import oracle
 from sparse_attention_top_idx_gb300 import workloads as wl
+from tests import test_oracle_fp4 as fp4pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "orc.c")
 
@@ -41,6 +42,13 @@ MUTANTS = {
     "bf16_round_half_up": ("u = u + 0x7FFFu + ((u >> 16) & 1u);", "u = u + 0x8000u;"),
     "translate_offset_dropped": ("out[i] = (int64_t)table_row[s / bs] * bs + s % bs;",
                                  "out[i] = (int64_t)table_row[s / bs] * bs;"),
+    "e2m1_ties_odd": ("if (dist < bd || (dist == bd && (c & 1) == 0)) {",
+                      "if (dist < bd || (dist == bd && (c & 1) == 1)) {"),
+    "e2m1_no_saturation": ("if (a >= orc_e2m1_mag[7])", "if (a > 1e30)"),
+    "fp4_block_64": ("#define ORC_FP4_BLOCK 32", "#define ORC_FP4_BLOCK 64"),
+    "fp4_max_4": ("s = amax / 6.0f;", "s = amax / 4.0f;"),
+    "fp4_scale_not_reapplied": ("y[b + j] = (float)(orc_e2m1_decode(orc_e2m1_encode(v)) * (double)s);",
+                                "y[b + j] = (float)(orc_e2m1_decode(orc_e2m1_encode(v)));"),
 }
 
 
@@ -123,6 +131,26 @@ def battery(O) -> bool:
         blk, off = divmod(int(slot), 64)
         if not np.array_equal(pool[blk * 8448 + off * 128: blk * 8448 + off * 128 + 128], c2[s_]):
             return False
+    # e2m1: every bf16 pattern against the decision boundaries
+    b = np.arange(1 << 16, dtype=np.uint32)
+    xb = (b << 16).view(np.float32)
+    xb = xb[np.isfinite(xb)]
+    if not np.array_equal(O.e2m1_encode(xb), fp4pins.encode_by_boundaries(xb)):
+        return False
+    # fp4 round trip: grid rows with power-of-two block scales are fixed points
+    codes = rng.integers(0, 16, (8, 128))
+    codes[:, ::32] = 7
+    e = rng.integers(-10, 10, (8, 4)).repeat(32, axis=1)
+    xg = (np.vectorize(fp4pins.e2m1_value)(codes) * 2.0 ** e).astype(np.float32)
+    if not np.array_equal(O.fp4_roundtrip_rows(xg), xg):
+        return False
+    # blocks are 32 wide and independent
+    xr = rng.standard_normal((4, 128)).astype(np.float32)
+    yr = O.fp4_roundtrip_rows(xr)
+    xo = xr.copy()
+    xo[:, 32] *= np.float32(1000.0)
+    if not np.array_equal(O.fp4_roundtrip_rows(xo)[:, :32], yr[:, :32]):
+        return False
     return True
 
 
