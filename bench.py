@@ -537,46 +537,54 @@ def bench_prefill(device, steps, warmup, peaks):
 
 
 def bench_precision(device):
-    """fp8 vs bf16 keys on the precision workload (4 sequences of 2000 / 4500 /
-    10000 / 22000 keys, one query each, planted needle), from the GPU's own
-    outputs: the needle's rank in each top-k (None: not selected), the
-    Jaccard overlap of the two index sets and the bf16 positions fp8 lost, at
-    top-512 and top-1024.  The pages' numbers for their own synthetic test
-    are attached as context."""
+    """Key formats against bf16 keys on the precision workload (4 sequences of
+    2000 / 4500 / 10000 / 22000 keys, one query each, planted needle), from the
+    GPU's own outputs: fp8 keys, fp8 keys after the fp4 round trip ("fp4"),
+    and the same with the Walsh-Hadamard rotation of keys (store) and queries
+    (caller side, fp64 on the device) ("rot_fp4").  Per format: the needle's
+    rank in each top-k (None: not selected), the Jaccard overlap with the
+    bf16 index set and the bf16 positions it lost, at top-512 and top-1024.
+    The pages' numbers for their own synthetic test are attached as context."""
     import torch
     from sparse_attention_top_idx_gb300 import dsaidx
     from sparse_attention_top_idx_gb300 import workloads as wl
-    from sparse_attention_top_idx_gb300.host import bf16_tensor, build_cache
+    from sparse_attention_top_idx_gb300.host import bf16_tensor, build_cache, hadamard_rotate_bf16
     rows = []
+    formats = (("bf16", dsaidx.BF16, False, False), ("fp8", dsaidx.FP8, False, False),
+               ("fp4", dsaidx.FP8, False, True), ("rot_fp4", dsaidx.FP8, True, True))
     for k in (512, 1024):
         W = wl.precision_compare(topk=k)
         idx = {}
-        for mode in (dsaidx.FP8, dsaidx.BF16):
-            cache = build_cache(W, mode, device=device)
+        for name, mode, rot, fp4 in formats:
+            cache = build_cache(W, mode, device=device, rotate=rot, fp4=fp4)
             B = W.batch
+            q = bf16_tensor(W.q, device)
+            if rot:
+                q = hadamard_rotate_bf16(q)
             ws = dsaidx.new_workspace(dsaidx.workspace_bytes_decode(cache, B, W.max_seq_len, W.H, k), device)
             oi = torch.empty((B, k), dtype=torch.int32, device=device)
-            dsaidx.score_topk_decode(cache, bf16_tensor(W.q, device), torch.from_numpy(W.w).to(device),
+            dsaidx.score_topk_decode(cache, q, torch.from_numpy(W.w).to(device),
                                      torch.from_numpy(W.block_table).to(device),
                                      torch.tensor(W.seq_lens, dtype=torch.int32, device=device),
                                      W.max_seq_len, k, oi, ws)
-            idx[mode] = oi.cpu().numpy()
+            idx[name] = oi.cpu().numpy()
             del cache, ws
         for b, S in enumerate(W.seq_lens):
-            f = [int(x) for x in idx[dsaidx.FP8][b] if x >= 0]
-            h = [int(x) for x in idx[dsaidx.BF16][b] if x >= 0]
             nd = int(W.needle_pos[b])
-            F, Hs = set(f), set(h)
+            sel = {n: [int(x) for x in idx[n][b] if x >= 0] for n, _, _, _ in formats}
+            Hs = set(sel["bf16"])
             row = {"S": int(S), "topk": k,
-                   "needle_rank_fp8": f.index(nd) + 1 if nd in F else None,
-                   "needle_rank_bf16": h.index(nd) + 1 if nd in Hs else None,
-                   "jaccard_fp8_vs_bf16": round(len(F & Hs) / max(1, len(F | Hs)), 4),
-                   "lost_bf16_to_fp8": len(Hs - F)}
+                   "needle_rank_bf16": sel["bf16"].index(nd) + 1 if nd in Hs else None}
+            for n in ("fp8", "fp4", "rot_fp4"):
+                F = set(sel[n])
+                row["needle_rank_" + n] = sel[n].index(nd) + 1 if nd in F else None
+                row["jaccard_%s_vs_bf16" % n] = round(len(F & Hs) / max(1, len(F | Hs)), 4)
+                row["lost_bf16_to_" + n] = len(Hs - F)
             if k == 512 and int(S) in PAGES_JACCARD_TOP512:
                 row["pages_jaccard"], row["pages_lost"] = PAGES_JACCARD_TOP512[int(S)]
             rows.append(row)
     torch.cuda.empty_cache()
-    return {"workload": "precision_s2000_4500_10000_22000", "source": "GPU outputs, both key formats",
+    return {"workload": "precision_s2000_4500_10000_22000", "source": "GPU outputs, every key format",
             "pages_context": "fp8-vs-bf16 top-512 Jaccard 0.395/0.382/0.299/0.267 at 2k/4.5k/10k/22k "
                              "from the pages' own synthetic test (different data)",
             "rows": rows}
@@ -689,7 +697,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the long-context and prefill objects")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--eager", action="store_true", help="no CUDA graphs (for profiler runs)")
-    ap.add_argument("--only", choices=["longctx", "prefill"], default=None,
+    ap.add_argument("--only", choices=["longctx", "prefill", "precision"], default=None,
                     help="run just one secondary workload and print its object (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -715,6 +723,9 @@ def main():
         return 0
     if args.only == "prefill":
         print(json.dumps(bench_prefill(device, args.steps, args.warmup, peaks)))
+        return 0
+    if args.only == "precision":
+        print(json.dumps(bench_precision(device)))
         return 0
 
     W = wl.decode_batch()

@@ -146,6 +146,30 @@ idx_status idx_store_keys_rotated(const idx_cache* cache, const void* k_bf16_dev
                                   const int64_t* slot_mapping_dev, int64_t n,
                                   int32_t* status_dev, void* stream);
 
+/* Options of idx_store_keys_ex. */
+#define IDX_STORE_ROTATE 1u          /* the Walsh-Hadamard rotation of idx_store_keys_rotated */
+#define IDX_STORE_FP4_ROUNDTRIP 2u   /* the fp4 round trip below, after the rotation if any */
+
+/*
+ * idx_store_keys with options (flags: IDX_STORE_* bits; 0 is idx_store_keys,
+ * IDX_STORE_ROTATE is idx_store_keys_rotated).  IDX_STORE_FP4_ROUNDTRIP puts
+ * the key through the quantisation-aware fp4 round trip that "DeepSeek-V4
+ * index_topk=1024 sparse indexer can't recall verbatim lines" (ROCm/ATOM
+ * issue #1507, section "Where (main 0c7d50f9)") lists on the indexer's key
+ * path after the rotation, fp4_act_quant_inplace(kv, 32): every block of 32
+ * consecutive values of the (rotated or bf16-widened) float row gets the
+ * scale s = fl32(amax / 6); each value x is replaced by fl32(c * s), c the
+ * e2m1 value (0, 0.5, 1, 1.5, 2, 3, 4, 6 with sign) nearest to fl32(x / s),
+ * a tie going to the even code and magnitudes beyond 6 to 6; a block of
+ * zeros is kept.  The resulting float row is then quantised (fp8) or rounded
+ * to bf16, nearest even, as for the rotated store.  Finite keys; same
+ * arguments, layout, ownership and errors as idx_store_keys, plus
+ * IDX_ERR_INVALID_ARG for unknown flag bits.
+ */
+idx_status idx_store_keys_ex(const idx_cache* cache, const void* k_bf16_dev,
+                             const int64_t* slot_mapping_dev, int64_t n, unsigned flags,
+                             int32_t* status_dev, void* stream);
+
 /*
  * Gather read of the cache (cp_gather_indexer_k_quant_cache in "DeepSeek-V4
  * index_topk=1024 sparse indexer can't recall verbatim lines", ROCm/ATOM issue

@@ -154,13 +154,13 @@ void idx_cache_destroy(idx_cache* cache) { delete cache; }
 
 namespace {
 idx_status store_keys_common(const idx_cache* cache, const void* k_bf16_dev, const int64_t* slot_mapping_dev,
-                             int64_t n, int32_t* status_dev, bool rotate, void* stream) {
-    if (!cache || n < 0) return IDX_ERR_INVALID_ARG;
+                             int64_t n, int32_t* status_dev, unsigned flags, void* stream) {
+    if (!cache || n < 0 || (flags & ~(IDX_STORE_ROTATE | IDX_STORE_FP4_ROUNDTRIP)) != 0u) return IDX_ERR_INVALID_ARG;
     if (n == 0) return IDX_OK;
     if (!k_bf16_dev || !slot_mapping_dev || !aligned(k_bf16_dev, 16) || !aligned(slot_mapping_dev, 8))
         return IDX_ERR_INVALID_ARG;
     if (!same_device(cache)) return IDX_ERR_INVALID_ARG;
-    cudaError_t e = dsaidx::launch_store(cache, k_bf16_dev, slot_mapping_dev, n, status_dev, rotate,
+    cudaError_t e = dsaidx::launch_store(cache, k_bf16_dev, slot_mapping_dev, n, status_dev, flags,
                                          static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
@@ -168,12 +168,17 @@ idx_status store_keys_common(const idx_cache* cache, const void* k_bf16_dev, con
 
 idx_status idx_store_keys(const idx_cache* cache, const void* k_bf16_dev, const int64_t* slot_mapping_dev,
                           int64_t n, int32_t* status_dev, void* stream) {
-    return store_keys_common(cache, k_bf16_dev, slot_mapping_dev, n, status_dev, false, stream);
+    return store_keys_common(cache, k_bf16_dev, slot_mapping_dev, n, status_dev, 0u, stream);
 }
 
 idx_status idx_store_keys_rotated(const idx_cache* cache, const void* k_bf16_dev, const int64_t* slot_mapping_dev,
                                   int64_t n, int32_t* status_dev, void* stream) {
-    return store_keys_common(cache, k_bf16_dev, slot_mapping_dev, n, status_dev, true, stream);
+    return store_keys_common(cache, k_bf16_dev, slot_mapping_dev, n, status_dev, IDX_STORE_ROTATE, stream);
+}
+
+idx_status idx_store_keys_ex(const idx_cache* cache, const void* k_bf16_dev, const int64_t* slot_mapping_dev,
+                             int64_t n, unsigned flags, int32_t* status_dev, void* stream) {
+    return store_keys_common(cache, k_bf16_dev, slot_mapping_dev, n, status_dev, flags, stream);
 }
 
 idx_status idx_gather_blocks(const idx_cache* cache, const int32_t* block_table_dev, int max_blocks_per_seq,

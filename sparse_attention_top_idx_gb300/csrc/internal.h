@@ -179,7 +179,7 @@ inline cudaError_t set_smem_once(Kern kern, int bytes, std::atomic<unsigned long
 
 // Kernel launchers (one per translation unit).
 cudaError_t launch_store(const idx_cache* c, const void* k, const int64_t* slots, int64_t n,
-                         int32_t* status, bool rotate, cudaStream_t st);
+                         int32_t* status, unsigned flags, cudaStream_t st);   // IDX_STORE_* flags
 cudaError_t launch_decode(const idx_cache* c, const ScoreParams& p, cudaStream_t st);
 cudaError_t launch_prefill(const idx_cache* c, const ScoreParams& p, cudaStream_t st);
 cudaError_t launch_gather(const idx_cache* c, const int32_t* block_table, int mbps, const int32_t* seq_lens,

@@ -23,6 +23,16 @@
 // exponents within 38 binades), then one multiply by the double nearest
 // 1/sqrt(128) and one rounding to float; the float row is quantised (fp8) or
 // rounded to bf16 (nearest even).
+//
+// fp4 round trip (IDX_STORE_FP4_ROUNDTRIP): after the optional rotation each
+// block of 32 values -- four lanes' worth -- takes the quantisation-aware
+// fp4 round trip that the same issue lists on the indexer's key path
+// (section "Where (main 0c7d50f9)", fp4_act_quant_inplace(kv, 32)): the
+// block's scale s = amax / 6 (correctly rounded), each x / s (correctly
+// rounded) goes to the nearest e2m1 magnitude by comparison with the
+// midpoints of the grid {0, 0.5, 1, 1.5, 2, 3, 4, 6} (a value on a midpoint
+// to the even code, beyond 6 to 6), and the decoded value times s (one fp32
+// rounding) replaces x before the quantisation or bf16 rounding.
 #include <cmath>
 
 #include "common.cuh"
@@ -65,13 +75,28 @@ __device__ __forceinline__ void wht128_halfwarp(double (&x)[8], int sub, unsigne
     }
 }
 
+// Magnitude of the e2m1 value nearest to a >= 0: the grid is 0, 0.5, 1,
+// 1.5, 2, 3, 4, 6 (codes 0..7); a value on the midpoint of two neighbours
+// takes the one with the even code, and everything from 5 up beyond the last
+// midpoint takes 6.
+__device__ __forceinline__ float e2m1_nearest(float a) {
+    if (a <= 0.25f) return 0.0f;   // midpoint 0 | 0.5: code 0
+    if (a < 0.75f) return 0.5f;    // 0.5 | 1: code 2 (1.0)
+    if (a <= 1.25f) return 1.0f;   // 1 | 1.5: code 2
+    if (a < 1.75f) return 1.5f;    // 1.5 | 2: code 4 (2.0)
+    if (a <= 2.5f) return 2.0f;    // 2 | 3: code 4
+    if (a < 3.5f) return 3.0f;     // 3 | 4: code 6 (4.0)
+    if (a <= 5.0f) return 4.0f;    // 4 | 6: code 6
+    return 6.0f;
+}
+
 // bf16 bits of a float, round to nearest even (finite values).
 __device__ __forceinline__ uint32_t bf16_rne(float f) {
     const uint32_t u = __float_as_uint(f);
     return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
 }
 
-template <bool kFp8, bool kRotate>
+template <bool kFp8, bool kRotate, bool kFp4>
 __global__ void __launch_bounds__(256) store_keys_kernel(const uint4* __restrict__ k,
                                                          const int64_t* __restrict__ slots,
                                                          int64_t n, uint8_t* __restrict__ pool,
@@ -117,8 +142,25 @@ __global__ void __launch_bounds__(256) store_keys_kernel(const uint4* __restrict
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[i] = __double2float_rn(__dmul_rn(xd[i], rot_scale));
         }
+        if constexpr (kFp4) {
+            // block of 32 = lanes 4b .. 4b + 3 of the half-warp
+            float bmax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) bmax = fmaxf(bmax, fabsf(x[i]));
+            bmax = fmaxf(bmax, __shfl_xor_sync(hmask, bmax, 1, 16));
+            bmax = fmaxf(bmax, __shfl_xor_sync(hmask, bmax, 2, 16));
+            if (bmax != 0.0f) {
+                const float s4 = __fdiv_rn(bmax, 6.0f);
+                const DivBy div4(s4);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float v = div4(x[i]);
+                    x[i] = __fmul_rn(copysignf(e2m1_nearest(fabsf(v)), v), s4);
+                }
+            }
+        }
         if constexpr (!kFp8) {
-            if constexpr (kRotate) {
+            if constexpr (kRotate || kFp4) {
                 const uint4 o = make_uint4(bf16_rne(x[0]) | (bf16_rne(x[1]) << 16), bf16_rne(x[2]) | (bf16_rne(x[3]) << 16),
                                            bf16_rne(x[4]) | (bf16_rne(x[5]) << 16), bf16_rne(x[6]) | (bf16_rne(x[7]) << 16));
                 reinterpret_cast<uint4*>(base + off * 256)[sub] = o;
@@ -156,7 +198,7 @@ __global__ void __launch_bounds__(256) store_keys_kernel(const uint4* __restrict
 }  // namespace
 
 cudaError_t launch_store(const idx_cache* c, const void* k, const int64_t* slots, int64_t n,
-                         int32_t* status, bool rotate, cudaStream_t st) {
+                         int32_t* status, unsigned flags, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
     const int64_t threads = n * 16;
     int64_t blocks = (threads + 255) / 256;
@@ -164,8 +206,14 @@ cudaError_t launch_store(const idx_cache* c, const void* k, const int64_t* slots
     if (blocks > cap) blocks = cap;
     const double rs = 1.0 / std::sqrt(static_cast<double>(kHeadDim));   // the double nearest 1/sqrt(128)
     const bool fp8 = c->key_dtype == IDX_KEY_FP8_E4M3;
-    auto kern = fp8 ? (rotate ? store_keys_kernel<true, true> : store_keys_kernel<true, false>)
-                    : (rotate ? store_keys_kernel<false, true> : store_keys_kernel<false, false>);
+    const bool rotate = (flags & IDX_STORE_ROTATE) != 0, fp4 = (flags & IDX_STORE_FP4_ROUNDTRIP) != 0;
+    using Kern = void (*)(const uint4*, const int64_t*, int64_t, uint8_t*, int64_t, int, int64_t, int32_t*, double);
+    static constexpr Kern kTable[8] = {
+        store_keys_kernel<false, false, false>, store_keys_kernel<false, true, false>,
+        store_keys_kernel<false, false, true>,  store_keys_kernel<false, true, true>,
+        store_keys_kernel<true, false, false>,  store_keys_kernel<true, true, false>,
+        store_keys_kernel<true, false, true>,   store_keys_kernel<true, true, true>};
+    const Kern kern = kTable[(fp8 ? 4 : 0) | (fp4 ? 2 : 0) | (rotate ? 1 : 0)];
     // programmatic serialization: the launch may overlap the previous kernel,
     // which the kernel waits for (griddepcontrol.wait) before any access
     cudaLaunchConfig_t cfg = {};

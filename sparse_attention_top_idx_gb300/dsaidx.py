@@ -56,6 +56,8 @@ def load(path: Optional[str] = None):
     L.idx_store_keys.restype = I
     L.idx_store_keys_rotated.argtypes = [P, P, P, I64, P, P]
     L.idx_store_keys_rotated.restype = I
+    L.idx_store_keys_ex.argtypes = [P, P, P, I64, ctypes.c_uint, P, P]
+    L.idx_store_keys_ex.restype = I
     L.idx_gather_blocks.argtypes = [P, P, I, P, I, P, P, P]
     L.idx_gather_blocks.restype = I
     L.idx_workspace_bytes_decode.argtypes = [P, I, I, I, I]
@@ -166,16 +168,27 @@ class IndexCache:
             pass
 
 
+STORE_ROTATE = 1
+STORE_FP4_ROUNDTRIP = 2
+
+
 def store_keys(cache: IndexCache, k_bf16: torch.Tensor, slot_mapping: torch.Tensor,
-               status: Optional[torch.Tensor] = None, stream=None, rotate: bool = False):
+               status: Optional[torch.Tensor] = None, stream=None, rotate: bool = False, fp4: bool = False):
     """idx_store_keys: quantise (fp8) or copy (bf16) n keys into their slots;
-    rotate=True: idx_store_keys_rotated (Walsh-Hadamard rotation first)."""
+    rotate=True: idx_store_keys_rotated (Walsh-Hadamard rotation first);
+    fp4=True: idx_store_keys_ex with the fp4 round trip (after the rotation)."""
     n = k_bf16.shape[0]
     _need(k_bf16, torch.bfloat16, "k_bf16", (n, HEAD_DIM))
     _need(slot_mapping, torch.int64, "slot_mapping", (n,))
     if status is not None:
         _need(status, torch.int32, "status")
-    fn = load().idx_store_keys_rotated if rotate else load().idx_store_keys
+    L = load()
+    if fp4:
+        flags = STORE_FP4_ROUNDTRIP | (STORE_ROTATE if rotate else 0)
+        _check(L.idx_store_keys_ex(cache.handle, _ptr(k_bf16), _ptr(slot_mapping), n, flags, _ptr(status),
+                                   _stream(stream)), "idx_store_keys_ex")
+        return
+    fn = L.idx_store_keys_rotated if rotate else L.idx_store_keys
     name = "idx_store_keys_rotated" if rotate else "idx_store_keys"
     _check(fn(cache.handle, _ptr(k_bf16), _ptr(slot_mapping), n, _ptr(status), _stream(stream)), name)
 

@@ -16,7 +16,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = dsaidx.header_functions()
-    assert len(names) == 19, names
+    assert len(names) == 20, names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -44,6 +44,7 @@ def test_host_argument_checks(lib):
     # calls on a null handle
     assert lib.idx_store_keys(None, None, None, 1, None, None) == 1
     assert lib.idx_store_keys_rotated(None, None, None, 1, None, None) == 1
+    assert lib.idx_store_keys_ex(None, None, None, 1, 2, None, None) == 1
     assert lib.idx_gather_blocks(None, None, 1, None, 1, None, None, None) == 1
     assert lib.idx_score_topk_decode(None, None, None, None, 1, None, 1, 1, 64, 8, None, None,
                                      None, 0, None) == 1

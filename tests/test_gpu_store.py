@@ -142,3 +142,66 @@ def test_rotated_keys_and_queries_score_parity(mode):
     check_rows(got, ref, pos + 1, W.topk)
     for b in range(B):
         assert got["idx"][b][0] == W.needle_pos[b]
+
+
+@pytest.mark.parametrize("rot", [False, True])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_fp4_roundtrip_store_bit_exact(mode, rot):
+    # idx_store_keys_ex with the fp4 round trip (after the rotation when rot)
+    # against the oracle's store, every byte; magnitudes spread over blocks
+    # and rows, zero blocks, a block whose values sit on e2m1 midpoints
+    W = wl.make_workload("stfp4", [1000, 77, 3000], [1, 1, 1], bs=64, seed=40 + mode + 2 * rot,
+                         extra_blocks=3)
+    k = W.all_keys().copy()
+    slots = W.all_slots().copy()
+    slots[::11] = -1
+    rng = np.random.default_rng(200 + mode + 2 * rot)
+    # per-block magnitudes without the rotation; with it one scale per row (the
+    # double-precision rotation is exact for rows within 38 binades)
+    scale = (10.0 ** rng.uniform(-20, 20, (k.shape[0], 1 if rot else 4))).astype(np.float32)
+    scale = scale.repeat(128 if rot else 32, axis=1)
+    kf = wl.bf16_bits_to_f32(k) * scale
+    kf[5] = 0.0
+    kf[6, 32:64] = 0.0
+    kf[8, :32] = np.array([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0] * 4, np.float32) * np.float32(0.5)
+    k = wl.f32_to_bf16_bits(kf)
+    cache = dsaidx.IndexCache.allocate(W.num_blocks, 64, mode, fill=0x5A)
+    dsaidx.store_keys(cache, bf16_tensor(k), torch.from_numpy(slots).cuda(), rotate=rot, fp4=True)
+    got = cache.pool.cpu().numpy()
+    want = np.full(W.num_blocks * oracle.block_bytes(mode, 64), 0x5A, np.uint8)
+    oracle.store_keys(want, k, slots, 64, mode, rotate=rot, fp4=True)
+    diff = np.nonzero(got != want)[0]
+    assert diff.size == 0, "first differing byte %d of %d" % (diff[0], diff.size)
+
+
+def test_store_ex_rejects_unknown_flags():
+    W = wl.make_workload("stflag", [10], [1], bs=64, seed=3)
+    cache = dsaidx.IndexCache.allocate(W.num_blocks, 64, 0, fill=0)
+    rc = dsaidx.load().idx_store_keys_ex(cache.handle, bf16_tensor(W.all_keys()).data_ptr(),
+                                         torch.from_numpy(W.all_slots()).cuda().data_ptr(), 10, 4, None, None)
+    assert rc == 1
+
+
+@pytest.mark.parametrize("rot", [False, True])
+def test_fp4_keys_score_parity(rot):
+    # keys stored through the fp4 round trip (fp8 pool), queries rotated by
+    # the caller when the keys are: decode parity against the oracle on the
+    # same operands
+    from tests.parity import check_rows, decode_inputs
+    W = wl.make_workload("fp4dec", [3000, 9000, 129], [1, 1, 1], topk=256, seed=51 + rot)
+    B, H, d = W.q.shape
+    q = oracle.f32_to_bf16(oracle.wht_rows(W.q.reshape(B * H, d))).reshape(B, H, d) if rot else W.q
+    cache = dsaidx.IndexCache.allocate(W.num_blocks, W.bs, 0, fill=0)
+    dsaidx.store_keys(cache, bf16_tensor(W.all_keys()), torch.from_numpy(W.all_slots()).cuda(), rotate=rot,
+                      fp4=True)
+    ins = decode_inputs(W)
+    ws = dsaidx.new_workspace(dsaidx.workspace_bytes_decode(cache, B, W.max_seq_len, H, W.topk))
+    oi = torch.full((B, W.topk), -7, dtype=torch.int32, device="cuda")
+    osc = torch.full((B, W.topk), float("nan"), dtype=torch.float32, device="cuda")
+    dsaidx.score_topk_decode(cache, bf16_tensor(q), ins["w"], ins["block_table"], ins["seq_lens"],
+                             W.max_seq_len, W.topk, oi, ws, out_score=osc)
+    got = {"idx": oi.cpu().numpy(), "score": osc.cpu().numpy()}
+    keys = [oracle.stored_key_rows(W.keys[b], 0, rotate=rot, fp4=True) for b in range(B)]
+    pos = np.asarray(W.seq_lens, np.int64) - 1
+    ref = oracle.score_topk(0, W.topk, q, W.w, np.arange(B, dtype=np.int32), pos, keys, full_scores=True)
+    check_rows(got, ref, pos + 1, W.topk)
