@@ -305,16 +305,20 @@ __global__ void __maxnreg__(96)
         // the other waits for its next accumulator.  Epilogue warp e = w - 4
         // reads TMEM lane quadrant qd = w % 4 (32 keys) for queries
         // 2 (e / 8) and 2 (e / 8) + 1 of the group; each lane keeps the
-        // weights of its 16 heads of both queries in registers and writes the
-        // scores of quadrant row head_sum_row(lane).
+        // weights of its 16 heads of both queries in registers (reloading
+        // the second query's per tile measured 4 % slower than the spill of
+        // 24 bytes that holding both costs; key scales in a shared-memory ring
+        // instead of the prefetch below, 15 % slower) and writes the scores
+        // of quadrant row head_sum_row(lane).
         const int e = warp - 4;
         const int qd = warp & 3;
         const int g = (e >> 2) & 1;
         const int jq = 2 * (e >> 3);
         const int orow = qd * 32 + head_sum_row(lane);
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(qd * 32) << 16);
-        unsigned long long wr0[8];
+        unsigned long long wr0[8], wr1[8];
         load_head_weights(wq + jq * 64, lane, wr0);
+        load_head_weights(wq + (jq + 1) * 64, lane, wr1);
         const int vis0 = jq < ks->nrows ? ks->pos[jq] : -1;
         const int vis1 = jq + 1 < ks->nrows ? ks->pos[jq + 1] : -1;
         float* out0 = p.scores + static_cast<int64_t>(ks->row0 + jq) * p.score_stride;
@@ -334,20 +338,17 @@ __global__ void __maxnreg__(96)
                                                             kBs * 128) + (key % kBs));
             }
         };
-        float sc0 = scale_of(g), sc1 = scale_of(g + 2);
+        float sc0 = scale_of(g);
         for (int t = g; t < ntiles; t += 2) {
             const uint32_t aph = static_cast<uint32_t>(t >> 1) & 1u;
             const float kscale = sc0;
-            sc0 = sc1;
-            sc1 = scale_of(t + 4);
+            sc0 = scale_of(t + 2);
             // waits are combined over the warp so that every lane leaves together
             if (!__all_sync(0xffffffffu, mbar_wait(&tfull[g], aph, status, &ks->abort, p.wait_ns))) break;
             tc_fence_after();
             const uint32_t col = lane_base + static_cast<uint32_t>(g * kN + jq * 64);
             const float h0 = head_sum_rows(col, wr0, lane, [] {});
             // every TMEM read of the buffer by this warp has completed when release runs
-            unsigned long long wr1[8];
-            load_head_weights(wq + (jq + 1) * 64, lane, wr1);
             const float h1 = head_sum_rows(col + 64, wr1, lane, [&] {
                 tc_fence_before();
                 __syncwarp();
