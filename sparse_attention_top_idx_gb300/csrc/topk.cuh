@@ -322,25 +322,19 @@ __device__ uint64_t radix_refine(Each each, int bin, uint32_t m, SelectSmem* ss)
 }
 
 // ---------------------------------------------------------------------------
-// Rank sort, descending, of up to 256 * E composites (all 256 threads).
+// Merge sort, descending, of up to 256 * E composites (all 256 threads).
 // Each warp sorts a run of 32 * E composites in registers (bitonic network,
 // E per lane, lane l holding run positions l*E .. l*E+E-1: compare-exchanges
 // between a lane's registers, then across lanes by shuffles, no block
-// barriers).  The runs go to shared memory and every composite's final
-// position is its position in its own run plus, for each of the seven other
-// runs, the number of its members that are larger (binary searches).
-// Composites are unique, so the positions are a permutation; zero is the
-// padding value and is never written back.  This code runs once per block
-// from a cold instruction cache, so its loops stay rolled: the code is small
-// and each instruction is fetched once, then re-issued from the cache.
+// barriers).  Three merge-path levels then merge the eight runs pairwise
+// (8 -> 4 -> 2 -> 1): each thread finds, by a binary search on its output
+// diagonal, how many of its first output's predecessors come from each run
+// of its pair and merges its E outputs sequentially.  Zero is the padding
+// value: positions at or beyond n hold zeros at every level (the zeros sort
+// last), so they are neither read nor written.  This code runs once per
+// block from a cold instruction cache, so its loops stay rolled: the code is
+// small and each instruction is fetched once, then re-issued from the cache.
 // ---------------------------------------------------------------------------
-
-// Address of run position j in a run stored lane-transposed (position
-// l*E + e of a warp's registers at word e*32 + l).
-template <int E>
-__device__ __forceinline__ int run_slot(int j) {
-    return (j % E) * 32 + j / E;
-}
 
 template <int E>
 __device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[E], int lane) {
@@ -380,11 +374,11 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[E], int lane) {
     }
 }
 
-// Sorts a[0 .. n) descending, n <= 256 * E; `runs` is scratch for 256 * E
+// Sorts a[0 .. n) descending, n <= 256 * E; `runs` is scratch for n
 // composites that must not overlap a.
 template <int E>
-__device__ __forceinline__ void block_rank_sort(uint64_t* a, int n, uint64_t* runs) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+__device__ __forceinline__ void block_merge_sort(uint64_t* a, int n, uint64_t* runs) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, tid = threadIdx.x;
     constexpr int R = 32 * E;
     {
         uint64_t v[E];
@@ -394,49 +388,61 @@ __device__ __forceinline__ void block_rank_sort(uint64_t* a, int n, uint64_t* ru
             v[e] = i < n ? a[i] : 0ull;
         }
         warp_sort_desc<E>(v, lane);
-        uint64_t* mine = runs + w * R;
 #pragma unroll
-        for (int e = 0; e < E; ++e) mine[e * 32 + lane] = v[e];
+        for (int e = 0; e < E; ++e) {
+            const int j = w * R + lane * E + e;
+            if (j < n) runs[j] = v[e];
+        }
     }
-    __syncthreads();
-    // final position = own run position + larger members of the 7 other runs
-    // (seven branch-free binary searches advanced together)
+    // runs -> a -> runs -> a; a pair of runs of length L starts at 2 L p
+    uint64_t* src = runs;
+    uint64_t* dst = a;
 #pragma unroll 1
-    for (int e = 0; e < E; ++e) {
-        const int j0 = lane * E + e;
-        const uint64_t x = runs[w * R + run_slot<E>(j0)];
-        if (x == 0ull) continue;     // padding (zeros sort last in each run)
-        int pos[7];
+    for (int L = R; L < 8 * R; L <<= 1) {
+        __syncthreads();
+        const int g0 = tid * E;                  // this thread's first output
+        if (g0 < n) {
+            const int base = g0 & ~(2 * L - 1);
+            const int d = g0 - base;
+            const uint64_t* A = src + base;
+            const uint64_t* B = A + L;
+            const int na = max(0, min(L, n - base)), nb = max(0, min(L, n - base - L));
+            auto av = [&](int i) { return i < na ? A[i] : 0ull; };
+            auto bv = [&](int j) { return j < nb ? B[j] : 0ull; };
+            // i = outputs of [base, g0) that come from A (ties go to B first)
+            int lo = max(0, d - L), hi = min(d, L);
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (av(mid) > bv(d - 1 - mid)) lo = mid + 1;
+                else hi = mid;
+            }
+            int i = lo, j = d - lo;
+            uint64_t x = av(i), y = bv(j);
 #pragma unroll
-        for (int o = 0; o < 7; ++o) pos[o] = 0;
-#pragma unroll 1
-        for (int step = R / 2; step >= 1; step >>= 1) {
-#pragma unroll
-            for (int o = 0; o < 7; ++o) {
-                const uint64_t* other = runs + ((w + 1 + o) & 7) * R;
-                if (other[run_slot<E>(pos[o] + step - 1)] > x) pos[o] += step;
+            for (int e = 0; e < E; ++e) {
+                if (g0 + e >= n) break;
+                const bool ta = j >= L || (i < L && x > y);
+                dst[g0 + e] = ta ? x : y;
+                if (ta) x = av(++i);
+                else y = bv(++j);
             }
         }
-        int rank = j0;
-#pragma unroll
-        for (int o = 0; o < 7; ++o) {
-            const uint64_t* other = runs + ((w + 1 + o) & 7) * R;
-            rank += pos[o] + ((other[run_slot<E>(pos[o])] > x) ? 1 : 0);
-        }
-        a[rank] = x;
+        uint64_t* t = src;
+        src = dst;
+        dst = t;
     }
     __syncthreads();
 }
 
 // Sorts a[0 .. n) descending for n <= 256 * kMaxE (zero entries are padding
-// and must not occur among the n); `runs`: scratch for 256 * kMaxE
-// composites, disjoint from a.
+// and must not occur among the n); `runs`: scratch for n composites,
+// disjoint from a.
 template <int kMaxE>
 __device__ __forceinline__ void block_sort_desc_r(uint64_t* a, int n, uint64_t* runs) {
-    if (n <= 256) block_rank_sort<1>(a, n, runs);
-    else if (n <= 512 || kMaxE < 4) block_rank_sort<(kMaxE < 2 ? kMaxE : 2)>(a, n, runs);
-    else if (n <= 1024 || kMaxE < 8) block_rank_sort<(kMaxE < 4 ? kMaxE : 4)>(a, n, runs);
-    else block_rank_sort<kMaxE>(a, n, runs);
+    if (n <= 256) block_merge_sort<1>(a, n, runs);
+    else if (n <= 512 || kMaxE < 4) block_merge_sort<(kMaxE < 2 ? kMaxE : 2)>(a, n, runs);
+    else if (n <= 1024 || kMaxE < 8) block_merge_sort<(kMaxE < 4 ? kMaxE : 4)>(a, n, runs);
+    else block_merge_sort<kMaxE>(a, n, runs);
 }
 
 // Sort by counting, for short lists: the position of a[i] is the number of
