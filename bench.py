@@ -45,9 +45,9 @@ N_POOL_COPIES = 9
 # hash of the measured kernel's sources (its translation unit and every header
 # it includes) when they were taken; a stale hash reports null.
 NCU_TRAFFIC = {
-    ("decode", "b1064f746bcec8b2"): 31446272 + 0,
-    ("longctx", "b1064f746bcec8b2"): 277238272 + 2780160,
-    ("prefill", "53c45c72bce93128"): 139622144 + 531330560,   # the scoring kernel
+    ("decode", "bb140c876d0635fc"): 31442944 + 0,
+    ("longctx", "bb140c876d0635fc"): 277235456 + 2468864,
+    ("prefill", "017fe99aa3fc0084"): 139604992 + 537155840,   # the scoring kernel
 }
 KERNEL_TU = {"decode": "decode.cu", "longctx": "decode.cu", "prefill": "prefill.cu"}
 
