@@ -272,3 +272,21 @@ def test_large_batch_many_units_per_cluster(mode):
     for b in range(W.batch):
         if W.seq_lens[b] == 0:
             assert np.all(got["idx"][b] == -1)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_two_segment_merge_one_run_empty(mode):
+    # two-segment sequences whose second (first) segment's keys are scaled
+    # down a hundredfold, so one run contributes no candidate to the merge,
+    # a balanced one, and k not a multiple of 32
+    W = wl.make_workload("twoseg", [100000, 100000, 70000], [1, 1, 1], topk=1000, seed=61 + mode)
+    seg = 65536
+    for b, sl in ((0, slice(seg, None)), (1, slice(0, seg))):
+        kf = wl.bf16_bits_to_f32(W.keys[b])
+        kf[sl] *= np.float32(0.01)
+        W.keys[b] = wl.f32_to_bf16_bits(kf)
+    got = run_decode(W, mode)
+    check(W, mode, got)
+    assert np.all(got["idx"][0][got["idx"][0] >= 0] < seg)
+    # the first segment of row 1 holds the planted needle: at most it survives
+    assert np.sum(got["idx"][1][got["idx"][1] >= 0] < seg) <= 1
