@@ -685,47 +685,105 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
             if (flag) {
                 // a block id failed its check or a wait gave up: no selection
             } else if (fast) {
-                // ------------------------------------ 3. the pool, in every CTA: the
-                // candidates (bins at or above the boundary) bin by bin from the top,
-                // within a bin CTA by CTA; each CTA writes its own to their places
-                // in every pool, so no CTA sorts anything
+                // ------------------------------------ 3. the pool: the candidates
+                // (bins at or above the boundary) bin by bin from the top, within
+                // a bin CTA by CTA, the same layout in every CTA; CTA r ranks the
+                // places [r ctot / 8, (r + 1) ctot / 8) and reads only the bins
+                // that reach them, so each CTA writes a candidate to the pools of
+                // the CTAs whose places its bin reaches (mostly one), so no CTA
+                // sorts anything
                 const int wlo = static_cast<int>(gmax) - (kWinBins - 1);   // bin of thread 0
                 uint32_t* bstart = reinterpret_cast<uint32_t*>(a_tiles);     // [kWinBins] first place of a bin
                 uint32_t* blen = bstart + kWinBins;                          // [kWinBins] its entries
                 uint32_t* bfill = blen + kWinBins;                           // [kWinBins] this CTA's next place
+                // [kWinBins] CTAs whose places a bin reaches (bit mask), after the
+                // ranking's scratch (sub-bin counts, cursors, a crowded bin, list)
+                uint32_t* bdst = bfill + 4 * kWinBins + 2 * 2048 + kWinBins;
                 {
-                    uint32_t before = 0u;
+                    uint32_t before = 0u, mine = 0u;
 #pragma unroll
-                    for (int r = 0; r < kDecCl; ++r) before += r < static_cast<int>(rank) ? cr[r] : 0u;
+                    for (int r = 0; r < kDecCl; ++r) {
+                        before += r < static_cast<int>(rank) ? cr[r] : 0u;
+                        mine = r == static_cast<int>(rank) ? cr[r] : mine;
+                    }
                     bstart[tid] = after;
                     blen[tid] = hsum;
                     bfill[tid] = after + before;
+                    // owner of place x: the last r with r ctot / 8 <= x, (8 x + 7) / ctot
+                    uint32_t dm = 0u, recv = 0u;
+                    if (bt >= bstar && hsum > 0u) {
+                        const uint32_t ct = static_cast<uint32_t>(ctot);
+                        const uint32_t rf = (8u * after + 7u) / ct, rl = (8u * (after + hsum) - 1u) / ct;
+                        dm = ((2u << rl) - 1u) & ~((1u << rf) - 1u);
+                        if ((dm >> rank) & 1u) recv = hsum - mine;   // what the other CTAs send here
+                    }
+                    bdst[tid] = dm;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) recv += __shfl_xor_sync(0xffffffffu, recv, o);
+                    if (lane == 0) ks->sel.scratch[warp] = recv;
                 }
-                if (tid == 0) mbar_arrive_expect_tx(lbar, static_cast<uint32_t>(ctot - mycnt) * 8u);
                 __syncthreads();
+                if (tid == 0) {
+                    uint32_t e = 0u;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) e += ks->sel.scratch[q];
+                    mbar_arrive_expect_tx(lbar, e * 8u);
+                }
                 {
+                    // this CTA's candidates are first gathered into a list
+                    // (count per thread, scan, write: no atomics), then placed
+                    // one per thread, so that the atomic on a bin's next place
+                    // is not a dependent step of every candidate in turn
                     const uint32_t kthr = static_cast<uint32_t>(bstar) << kWinShift;   // smallest key of the boundary bin
                     const float4* s4 = reinterpret_cast<const float4*>(csc);
                     const int nj = (nkeys + 3) >> 2;
-                    auto place = [&](float v, int i) {
-                        const uint32_t key = score_key(v);
-                        if (i < nkeys && key >= kthr) {
-                            const uint64_t c = make_comp(key, key_begin + i);
-                            const uint32_t slot = atomicAdd(&bfill[static_cast<int>(win_bin(key)) - wlo], 1u);
-                            pool[slot] = c;
-#pragma unroll 1
-                            for (int q = 0; q < kDecCl - 1; ++q) {
-                                const uint32_t dst = static_cast<uint32_t>(q) + (static_cast<uint32_t>(q) >= rank ? 1u : 0u);
-                                dsmem_st_async_u64(dsmem_addr(pool + slot, dst), c, dsmem_addr(lbar, dst));
-                            }
-                        }
+                    auto is_cand = [&](float v, int i) { return i < nkeys && score_key(v) >= kthr; };
+                    uint32_t mc = 0u;
+                    for (int j = tid; j < nj; j += kThreads) {
+                        const float4 x = s4[j];
+                        mc += (is_cand(x.x, 4 * j) ? 1u : 0u) + (is_cand(x.y, 4 * j + 1) ? 1u : 0u) +
+                              (is_cand(x.z, 4 * j + 2) ? 1u : 0u) + (is_cand(x.w, 4 * j + 3) ? 1u : 0u);
+                    }
+                    uint32_t incl = mc;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    if (lane == 31) ks->sel.scratch[8 + warp] = incl;
+                    __syncthreads();
+                    uint32_t at = incl - mc, nlist = 0u;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const uint32_t x = ks->sel.scratch[8 + q];
+                        at += q < warp ? x : 0u;
+                        nlist += x;
+                    }
+                    // the list lives where the ranking's crowded-bin buffer goes later
+                    uint64_t* lst = reinterpret_cast<uint64_t*>(bfill + 3 * kWinBins);
+                    auto put = [&](float v, int i) {
+                        if (is_cand(v, i)) lst[at++] = make_comp(score_key(v), key_begin + i);
                     };
                     for (int j = tid; j < nj; j += kThreads) {
                         const float4 x = s4[j];
-                        place(x.x, 4 * j);
-                        place(x.y, 4 * j + 1);
-                        place(x.z, 4 * j + 2);
-                        place(x.w, 4 * j + 3);
+                        put(x.x, 4 * j);
+                        put(x.y, 4 * j + 1);
+                        put(x.z, 4 * j + 2);
+                        put(x.w, 4 * j + 3);
+                    }
+                    __syncthreads();
+                    for (int q = tid; q < static_cast<int>(nlist); q += kThreads) {
+                        const uint64_t c = lst[q];
+                        const int t = static_cast<int>(win_bin(comp_key(c))) - wlo;
+                        const uint32_t slot = atomicAdd(&bfill[t], 1u);
+                        uint32_t dm = bdst[t];
+                        if ((dm >> rank) & 1u) pool[slot] = c;
+                        dm &= ~(1u << rank);
+                        while (dm != 0u) {
+                            const uint32_t dst = static_cast<uint32_t>(__ffs(dm) - 1);
+                            dm &= dm - 1u;
+                            dsmem_st_async_u64(dsmem_addr(pool + slot, dst), c, dsmem_addr(lbar, dst));
+                        }
                     }
                 }
                 const bool lok = __syncthreads_and(mbar_wait_cluster(lbar, lcnt & 1u, status, 2 * kWaitLimitNs));
