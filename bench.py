@@ -379,9 +379,13 @@ def e2e_decode(bench, steps, warmup, device):
     step copies the step's inputs host->device (queries, head weights, sequence
     lengths, the new keys and their slots, packed in one pinned buffer and sent
     as one copy), stores the keys, scores and selects, and copies the selected
-    indices back to the host.  Timed two ways: replayed from a CUDA graph (how a
-    serving decode loop issues it; E2E_REPLAYS replays of the K steps, the
-    median reported) and issued eagerly from Python call by call."""
+    indices back to the host.  The copies are the library's copy kernel
+    (idx_copy: the GPU reads and writes the pinned buffers over the host link,
+    launched like the score calls' kernels); the same steps with the copy
+    engine (cudaMemcpyAsync through PyTorch) are timed beside it.  Timed two
+    ways: replayed from a CUDA graph (how a serving decode loop issues it;
+    E2E_REPLAYS replays of the K steps, the median reported) and issued eagerly
+    from Python call by call."""
     import torch
     W = bench.W
     h_in, d_in, (d_q, d_w, d_sl, d_k, d_s) = pack_pinned(
@@ -391,36 +395,49 @@ def e2e_decode(bench, steps, warmup, device):
     d2h = h_out.numel() * h_out.element_size()
     ds = bench.dsaidx
 
-    def one(i, ev=None):
-        c = bench.caches[i % len(bench.caches)]
-        d_in.copy_(h_in, non_blocking=True)
-        ds.store_keys(c, d_k, d_s)
-        ds.score_topk_decode(c, d_q, d_w, bench.bt, d_sl, bench.msl, W.topk, bench.out, bench.ws)
-        h_out.copy_(bench.out, non_blocking=True)
+    def make_one(engine):
+        def one(i, ev=None):
+            c = bench.caches[i % len(bench.caches)]
+            if engine:
+                d_in.copy_(h_in, non_blocking=True)
+            else:
+                ds.copy(d_in, h_in)
+            ds.store_keys(c, d_k, d_s)
+            ds.score_topk_decode(c, d_q, d_w, bench.bt, d_sl, bench.msl, W.topk, bench.out, bench.ws)
+            if engine:
+                h_out.copy_(bench.out, non_blocking=True)
+            else:
+                ds.copy(h_out, bench.out)
+        return one
 
-    for i in range(warmup):
-        one(i)
-    torch.cuda.synchronize(device)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    g = capture(one, steps, warmup, device)
-    g.replay()
-    torch.cuda.synchronize(device)
-    reps = []
-    for _ in range(E2E_REPLAYS):
-        a.record()
+    res = {}
+    for engine in (False, True):
+        one = make_one(engine)
+        for i in range(warmup):
+            one(i)
+        torch.cuda.synchronize(device)
+        g = capture(one, steps, warmup, device)
         g.replay()
+        torch.cuda.synchronize(device)
+        reps = []
+        for _ in range(E2E_REPLAYS):
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize(device)
+            reps.append(a.elapsed_time(b) / steps)
+        del g
+        a.record()
+        for i in range(steps):
+            one(warmup + i)
         b.record()
         torch.cuda.synchronize(device)
-        reps.append(a.elapsed_time(b) / steps)
-    ms_graph = float(np.median(reps))
-    a.record()
-    for i in range(steps):
-        one(warmup + i)
-    b.record()
-    torch.cuda.synchronize(device)
-    ms_eager = a.elapsed_time(b) / steps
-    return ms_graph, ms_eager, h2d, d2h, reps
+        res[engine] = (float(np.median(reps)), a.elapsed_time(b) / steps, reps)
+    # the last step's indices, copied by the kernel, equal the device's
+    assert torch.equal(h_out, bench.out.cpu())
+    return res[False][0], res[False][1], h2d, d2h, res[False][2], res[True][0]
 
 
 def roofline_hbm(algo_bytes, kern_ms, peak_gbs, traffic):
@@ -741,9 +758,10 @@ def main():
     ms_step = total_ms / args.steps
     value = whole_job_rate(world, bench.keys, ms_step)
 
-    e2e_ms, e2e_eager_ms, h2d, d2h, e2e_reps = e2e_decode(bench, args.steps, args.warmup, device)
+    e2e_ms, e2e_eager_ms, h2d, d2h, e2e_reps, e2e_engine_ms = e2e_decode(bench, args.steps, args.warmup, device)
     e2e_ms = max_over_ranks(e2e_ms, dist, device)
     e2e_eager_ms = max_over_ranks(e2e_eager_ms, dist, device)
+    e2e_engine_ms = max_over_ranks(e2e_engine_ms, dist, device)
 
     tr = traffic_of("decode")
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -762,6 +780,8 @@ def main():
             "e2e": {"value": round(whole_job_rate(world, bench.keys, e2e_ms), 1), "unit": UNIT,
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "issue": "public API calls replayed from a CUDA graph",
+                    "copies": "idx_copy kernel (the GPU reads and writes the pinned host buffers)",
+                    "copy_engine_ms_per_step": round(e2e_engine_ms, 5),
                     "replays": len(e2e_reps), "ms_per_step_each_replay": [round(x, 5) for x in e2e_reps],
                     "eager_value": round(whole_job_rate(world, bench.keys, e2e_eager_ms), 1),
                     "eager_ms_per_step": round(e2e_eager_ms, 5)},

@@ -363,6 +363,18 @@ idx_status idx_test_set_wait_limit(unsigned long long limit_ns);
 int idx_kernel_timing(int capacity);
 int idx_kernel_times(float* out_ms, int max);
 
+/*
+ * (Library utility; no passage.)  Copies `bytes` from src to dst with a
+ * kernel on `stream`, for staging a step's inputs and results: each pointer is
+ * device memory, pinned host memory (used through its device alias), or, on a
+ * device that reads host page tables, any host memory; both 16-byte aligned
+ * and bytes a multiple of 16.  Launched like the score calls' kernels
+ * (programmatic serialization: it may be scheduled while the previous kernel
+ * in the stream finishes, and waits for it before touching memory).  Errors:
+ * IDX_ERR_INVALID_ARG (null, misaligned or unreachable pointers), IDX_ERR_CUDA.
+ */
+idx_status idx_copy(void* dst, const void* src, size_t bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -84,6 +84,8 @@ def load(path: Optional[str] = None):
     L.idx_test_set_wait_limit.restype = I
     L.idx_kernel_timing.argtypes = [ctypes.c_int]
     L.idx_kernel_timing.restype = ctypes.c_int
+    L.idx_copy.argtypes = [P, P, SZ, P]
+    L.idx_copy.restype = I
     L.idx_kernel_times.argtypes = [ctypes.c_void_p, ctypes.c_int]
     L.idx_kernel_times.restype = ctypes.c_int
     if path is None:
@@ -329,6 +331,17 @@ def test_set_wait_limit(limit_ns: int = 0):
     """idx_test_set_wait_limit: shorten the decode kernel's pipeline waits (and
     withhold one MMA signal) so that the timeout path runs; 0 restores."""
     _check(load().idx_test_set_wait_limit(int(limit_ns)), "idx_test_set_wait_limit")
+
+
+def copy(dst: torch.Tensor, src: torch.Tensor, stream=None):
+    """idx_copy: copy src into dst (same byte size, contiguous; device or
+    pinned host tensors) with the library's copy kernel."""
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("copy wants contiguous tensors")
+    nb = dst.numel() * dst.element_size()
+    if nb != src.numel() * src.element_size():
+        raise ValueError("copy wants equal byte sizes")
+    _check(load().idx_copy(_ptr(dst), _ptr(src), nb, _stream(stream)), "idx_copy")
 
 
 def kernel_timing(capacity: int) -> int:

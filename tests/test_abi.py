@@ -16,7 +16,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = dsaidx.header_functions()
-    assert len(names) == 20, names
+    assert len(names) == 21, names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -57,5 +57,7 @@ def test_host_argument_checks(lib):
     assert lib.idx_test_set_wait_limit(0) == 0     # restores the normal limit
     assert lib.idx_kernel_timing(0) == 0            # timing off: no events
     assert lib.idx_kernel_times(None, 0) == 0
+    assert lib.idx_copy(None, None, 16, None) == 1   # null pointers
+    assert lib.idx_copy(ctypes.c_void_p(16), ctypes.c_void_p(32), 8, None) == 1   # size not a multiple of 16
     assert dsaidx.status_str(0) == "ok"
     assert dsaidx.status_str(4) == "workspace too small"

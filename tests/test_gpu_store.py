@@ -205,3 +205,19 @@ def test_fp4_keys_score_parity(rot):
     pos = np.asarray(W.seq_lens, np.int64) - 1
     ref = oracle.score_topk(0, W.topk, q, W.w, np.arange(B, dtype=np.int32), pos, keys, full_scores=True)
     check_rows(got, ref, pos + 1, W.topk)
+
+
+def test_copy_kernel_host_device_round_trip():
+    # idx_copy from pinned host memory to the device and back, and device to
+    # device, byte for byte
+    rng = np.random.default_rng(5)
+    h = torch.from_numpy(rng.integers(0, 256, 541184, dtype=np.uint8)).pin_memory()
+    d = torch.empty(h.numel(), dtype=torch.uint8, device="cuda")
+    d2 = torch.empty_like(d)
+    back = torch.empty_like(h).pin_memory()
+    dsaidx.copy(d, h)
+    dsaidx.copy(d2, d)
+    dsaidx.copy(back, d2)
+    torch.cuda.synchronize()
+    assert torch.equal(back, h)
+    assert torch.equal(d.cpu(), h)
