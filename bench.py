@@ -42,19 +42,29 @@ N_POOL_COPIES = 9
 
 # DRAM bytes per launch of the dominant kernels from ncu captures
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
-# hash of the measured kernel's sources (its translation unit and every header
-# it includes) when they were taken; a stale hash reports null.
+# hash of the measured kernel's code (its translation unit and every header it
+# includes, comments left out) when they were taken; a stale hash reports null.
 NCU_TRAFFIC = {
-    ("decode", "fd7bc24dc85531ba"): 31444736 + 0,
-    ("longctx", "fd7bc24dc85531ba"): 277245696 + 2812160,
-    ("prefill", "017fe99aa3fc0084"): 139604992 + 537155840,   # the scoring kernel
+    ("decode", "6fbedace779f98ca"): 31444736 + 0,
+    ("longctx", "6fbedace779f98ca"): 277245696 + 2812160,
+    ("prefill", "1dd4133fc7337444"): 139604992 + 537155840,   # the scoring kernel
 }
 KERNEL_TU = {"decode": "decode.cu", "longctx": "decode.cu", "prefill": "prefill.cu"}
 
 
+def _code_only(text: str) -> str:
+    """A source with its comments and blank lines removed (string literals in
+    these sources hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(tu: str) -> str:
     """sha256 (first 16 hex digits) of a kernel translation unit and the
-    closure of the quoted headers it includes (csrc/ and include/)."""
+    closure of the quoted headers it includes (csrc/ and include/), comments
+    and blank lines left out."""
     dirs = [os.path.join(ROOT, "sparse_attention_top_idx_gb300", "csrc"), os.path.join(ROOT, "include")]
     seen, todo = [], [tu]
     while todo:
@@ -74,8 +84,8 @@ def kernel_source_hash(tu: str) -> str:
     for name in sorted(seen):
         path = next(os.path.join(d, name) for d in dirs if os.path.exists(os.path.join(d, name)))
         h.update(name.encode())
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -31,11 +31,12 @@
 //              w' to the other 7 CTAs (bulk shared-to-shared copies counted
 //              on their query barrier), so the B tile is built once per
 //              cluster;
-//   warps 4-7  run the epilogue: one key row per thread, 16 TMEM columns at a
-//              time, ks[s] * sum_h w'[h] * max(D, 0) with the head weights in
-//              registers and the key scale loaded from the cache two tiles
-//              ahead; the score goes to shared memory and into a histogram of
-//              the chunk at 1/32 octave (score key >> 19).
+//   warps 4-7  run the epilogue (head_sum_rows: each lane sums 16 of the 64
+//              heads of four key rows from .16x256b TMEM loads, a shuffle
+//              step leaves it one row's sum), ks[s] * sum_h w'[h] * max(D, 0)
+//              with the head weights in registers and the key scale loaded
+//              from the cache two tiles ahead; the score goes to shared memory
+//              and into a histogram of the chunk at 1/32 octave (score key >> 19).
 // Selection, by the 8 CTAs together with two one-way exchanges (st.async,
 // counted on the receiver's mbarrier; a remote shared-memory load would cost
 // a round trip):

@@ -264,7 +264,7 @@ __device__ __noinline__ int seg_select(const Set walk, int k, uint32_t* hist, ui
 // (thread t holds bins 16 t .. 16 t + 15 in registers); every element is
 // scattered to its bin's next place in tmp and then placed by its rank inside
 // its bin (bins hold a few elements for spread keys).  A bin of more than 64
-// elements (many equal or very close keys) sends the set to the rank sort.
+// elements (many equal or very close keys) sends the set to the block sort.
 // hist, cur: 4096 words each; tmp: n composites (disjoint from a).  All 256
 // threads.
 __device__ __noinline__ void bin_order(uint64_t* a, int n, uint64_t* tmp, uint32_t lo, uint32_t hi, uint32_t* hist,
