@@ -36,7 +36,7 @@
 //              step leaves it one row's sum), ks[s] * sum_h w'[h] * max(D, 0)
 //              with the head weights in registers and the key scale loaded
 //              from the cache two tiles ahead; the score goes to shared memory
-//              and into a histogram of the chunk at 1/32 octave (score key >> 19).
+//              and into a histogram of the chunk at 1/16 octave (score key >> 19).
 // Selection, by the 8 CTAs together with two one-way exchanges (st.async,
 // counted on the receiver's mbarrier; a remote shared-memory load would cost
 // a round trip):
@@ -877,14 +877,13 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                     if (ks->last) {
                         // ------------------------------------ sequence merge
                         __threadfence();
-                        const bool bad = __ldcg(p.seqflag + b) != 0u;
-                        int mout = -1;
-                        if (!bad)
-                            mout = merge_runs(p.cand + static_cast<int64_t>(b) * p.cand_cap, nseg, k, gh, shist,
-                                              reinterpret_cast<uint32_t*>(pool), sbuf, &ks->sel);
+                        // (-1: a segment failed a device check; merge_runs also
+                        // leaves the histogram zeroed)
+                        const int mout = merge_runs(p.cand + static_cast<int64_t>(b) * p.cand_cap, nseg, k, gh,
+                                                    p.seqflag + b, shist, reinterpret_cast<uint32_t*>(pool), sbuf,
+                                                    &ks->sel);
                         write_topk_row(sbuf, mout, k, oi, os, osl, btr, p.mbps, kBs);
-                        // leave the sequence's workspace zeroed for the next call
-                        for (int i = tid; i < kGHistWords; i += kThreads) gh[i] = 0u;
+                        // leave the rest of the sequence's workspace zeroed for the next call
                         if (tid == 0) {
                             p.ctr[b] = 0u;
                             p.seqflag[b] = 0u;

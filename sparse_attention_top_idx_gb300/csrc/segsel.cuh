@@ -18,9 +18,9 @@
 //  5. when the collected set is much larger than k (many equal or near-equal
 //     scores), refine the boundary bin by 8-bit digits of the composite;
 //  6. sort the collected composites and map the winners' keys back.
-// bin_order / small_select: a sorted order of at most 2048 composites by
-// mapped bins and ranks inside a bin.  merge_runs: the top-k of a long
-// sequence from its segments' sorted runs.
+// bin_order: a sorted order of at most 2048 composites by mapped bins and
+// ranks inside a bin.  merge_runs: the top-k of a long sequence from its
+// segments' sorted runs.
 #pragma once
 
 #include "common.cuh"
@@ -259,33 +259,41 @@ __device__ __noinline__ int seg_select(const Set walk, int k, uint32_t* hist, ui
 // ---------------------------------------------------------------------------
 
 // Sorts the n composites of a[0, n) descending, n <= 2048, leaving them in
-// a[0, n); every key lies in [lo, hi].  The keys are mapped onto 32 bits over
-// that range and a 4096-bin histogram gives each bin its first output place
-// (thread t holds bins 16 t .. 16 t + 15 in registers); every element is
-// scattered to its bin's next place in tmp and then placed by its rank inside
-// its bin (bins hold a few elements for spread keys).  A bin of more than 64
-// elements (many equal or very close keys) sends the set to the block sort.
-// hist, cur: 4096 words each; tmp: n composites (disjoint from a).  All 256
-// threads.
+// a[0, n); every key is at least lo.  The keys in [lo, hi] are mapped onto 32
+// bits over that range, keys above hi go to the top bin (so a few outlying
+// large scores need not stretch the range that the rest share), and a
+// 4096-bin histogram gives each bin its first output place (thread t holds
+// bins 16 t .. 16 t + 15 in registers); every element is scattered to its
+// bin's next place in tmp and then placed by its rank inside its bin (bins
+// hold a few elements for spread keys).  A bin of more than 64 elements (many
+// equal or very close keys) sends the set to the block sort.  Bin b lives at
+// word b ^ ((b >> 3) & 12) of hist and cur, so that the 16-byte slots of
+// eight consecutive threads' bins fall on distinct banks.  hist, cur: 4096
+// words each; tmp: n composites (disjoint from a).  All 256 threads.
 __device__ __noinline__ void bin_order(uint64_t* a, int n, uint64_t* tmp, uint32_t lo, uint32_t hi, uint32_t* hist,
                                        uint32_t* cur, SegSelSmem* sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int z = hi > lo ? __clz(hi - lo) : 0;
-    auto bin_of = [&](uint64_t c) { return ((comp_key(c) - lo) << z) >> kHistShift; };
+    auto word_of = [&](uint64_t c) {
+        const uint32_t key = comp_key(c);
+        const uint32_t b = key > hi ? static_cast<uint32_t>(kHistBins - 1) : ((key - lo) << z) >> kHistShift;
+        return b ^ ((b >> 3) & 12u);
+    };
+    auto slot_of = [](uint32_t s) { return s ^ ((s >> 3) & 3u); };   // 16-byte slot s = 4 t + j
     {
         uint4* h4 = reinterpret_cast<uint4*>(hist);
         for (int i = tid; i < kHistBins / 4; i += kTopkThreads) h4[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
-    for (int i = tid; i < n; i += kTopkThreads) atomicAdd(&hist[bin_of(a[i])], 1u);
+    for (int i = tid; i < n; i += kTopkThreads) atomicAdd(&hist[word_of(a[i])], 1u);
     __syncthreads();
     // counts of this thread's 16 bins, their first places, the largest count
     uint32_t v[16];
     {
-        const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 4 * tid;
+        const uint4* h4 = reinterpret_cast<const uint4*>(hist);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint4 x = h4[j];
+            const uint4 x = h4[slot_of(static_cast<uint32_t>(4 * tid + j))];
             v[4 * j] = x.x;
             v[4 * j + 1] = x.y;
             v[4 * j + 2] = x.z;
@@ -330,67 +338,51 @@ __device__ __noinline__ void bin_order(uint64_t* a, int n, uint64_t* tmp, uint32
             st[j] = acc;
             acc += v[j];
         }
-        uint4* o4 = reinterpret_cast<uint4*>(hist) + 4 * tid;
-        uint4* c4 = reinterpret_cast<uint4*>(cur) + 4 * tid;
+        uint4* o4 = reinterpret_cast<uint4*>(hist);
+        uint4* c4 = reinterpret_cast<uint4*>(cur);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint4 x = make_uint4(st[4 * j], st[4 * j + 1], st[4 * j + 2], st[4 * j + 3]);
-            o4[j] = x;
-            c4[j] = x;
+            const uint32_t sl = slot_of(static_cast<uint32_t>(4 * tid + j));
+            o4[sl] = x;
+            c4[sl] = x;
         }
     }
     __syncthreads();
     // scatter every element to its bin's next place
     for (int i = tid; i < n; i += kTopkThreads) {
         const uint64_t c = a[i];
-        tmp[atomicAdd(&cur[bin_of(c)], 1u)] = c;
+        tmp[atomicAdd(&cur[word_of(c)], 1u)] = c;
     }
     __syncthreads();
-    // place every element by its rank inside its bin [hist[b], cur[b])
-    for (int i = tid; i < n; i += kTopkThreads) {
-        const uint64_t c = tmp[i];
-        const uint32_t b = bin_of(c);
-        const uint32_t e = cur[b];
-        uint32_t r = hist[b];
-        for (uint32_t j = r; j < e; ++j) r += tmp[j] > c ? 1u : 0u;
-        a[r] = c;
+    // place every element by its rank inside its bin [hist[w], cur[w]): the
+    // same trip counts in a warp (the rank loop runs to the warp's largest
+    // bin), bin mates read four at a time (a composite is never zero, so a
+    // zero in a lane past its bin's end counts nothing)
+    for (int i0 = 0; i0 < n; i0 += kTopkThreads) {
+        const int i = i0 + tid;
+        const bool ok = i < n;
+        const uint64_t c = ok ? tmp[i] : 0ull;
+        const uint32_t w = word_of(c);
+        const uint32_t s0 = ok ? hist[w] : 0u;
+        const uint32_t cnt = ok ? cur[w] - s0 : 0u;
+        const uint32_t m = __reduce_max_sync(0xffffffffu, cnt);
+        uint32_t r = s0;
+        for (uint32_t j = 0; j < m; j += 4) {
+            const uint64_t t0 = j < cnt ? tmp[s0 + j] : 0ull;
+            const uint64_t t1 = j + 1 < cnt ? tmp[s0 + j + 1] : 0ull;
+            const uint64_t t2 = j + 2 < cnt ? tmp[s0 + j + 2] : 0ull;
+            const uint64_t t3 = j + 3 < cnt ? tmp[s0 + j + 3] : 0ull;
+            r += (t0 > c ? 1u : 0u) + (t1 > c ? 1u : 0u) + (t2 > c ? 1u : 0u) + (t3 > c ? 1u : 0u);
+        }
+        if (ok) a[r] = c;
     }
     __syncthreads();
-}
-
-// Exact sorted top-k of the n composites c[0, n) (n <= 2048, in shared
-// memory): their key range, then bin_order; c[0, min(k, n)) then holds the
-// winners.  tmp: n composites; hist, cur: 4096 words.  All 256 threads.
-__device__ __noinline__ int small_select(uint64_t* c, int n, int k, uint64_t* tmp, uint32_t* hist, uint32_t* cur,
-                                         SegSelSmem* sm) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-    for (int i = tid; i < n; i += kTopkThreads) {
-        const uint32_t key = comp_key(c[i]);
-        lo = min(lo, key);
-        hi = max(hi, key);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-    }
-    if (lane == 0) {
-        sm->red[warp] = lo;
-        sm->red[8 + warp] = hi;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        lo = min(lo, sm->red[w]);
-        hi = max(hi, sm->red[8 + w]);
-    }
-    bin_order(c, n, tmp, lo, hi, hist, cur, sm);
-    return min(k, n);
 }
 
 // Histogram windows of the decode selection: bins of the score key at
-// 1/32 octave (key >> 19, 8192 bins over all keys); a CTA's window is the 256
+// 1/16 octave (key >> 19: sign, exponent and 4 mantissa bits; 8192 bins over
+// all keys); a CTA's window is the 256
 // bins below its largest score.
 constexpr int kWinShift = 19;
 constexpr int kWinBins = 256;                        // bins of a window, ending at the chunk's largest
@@ -482,99 +474,120 @@ __device__ __forceinline__ void rank_pool(const uint64_t* pool, int lo, int hi, 
 // Exact sorted top-k over the nseg sorted runs of k composites (zero-padded)
 // of one sequence, runs[j * k + e] in global memory, given the histogram gh
 // (kGHistWords words: kGHistBins bins of key >> 19 over every run entry, then
-// the largest bin + 1).  The boundary bin of the k-th largest entry comes from
-// the 256 bins below the largest (all 8192 bins when those hold fewer than k);
-// the candidates are each run's prefix at or above it (runs are sorted), read
-// in rounds: every open run's next R entries, R sized so that a round is about
-// 1024 loads over the block, a run staying open while its last read entry is a
-// candidate; bin_order sorts them over the key range the histogram gives.
-// With more than 2048 candidates, selects over all run entries (seg_select).
+// the largest bin + 1) and the sequence's device-check flag, read together
+// with the largest bin.  The boundary bin of the k-th largest entry comes
+// from the 256 bins below the largest (all 8192 bins when those hold fewer
+// than k), and so does the bin where the count from the top reaches
+// min(16, k); gh is then zeroed for the next call (every segment added its
+// counts before taking its ticket), the stores draining while the candidates
+// are read.  The candidates are each run's prefix at or above the boundary
+// (runs are sorted): with two runs, the two prefixes merged; else read in
+// rounds -- every open run's next R entries, R sized so that a round is about
+// 2048 loads over the block, a run staying open while its last read entry is
+// a candidate -- and put in order by bin_order over the key range from the
+// boundary bin to the top of the min(16, k) bin (the few entries above, such
+// as one planted far larger score, share the top bin).  With more than 2048
+// candidates, selects over all run entries (seg_select).
 // buf: >= 4096 composites; hist, cur: 4096 words.  Returns nout, buf[0, nout)
-// sorted descending.  All 256 threads.
-__device__ __noinline__ int merge_runs(const uint64_t* runs, int nseg, int k, const uint32_t* gh, uint32_t* hist,
-                                       uint32_t* cur, uint64_t* buf, SegSelSmem* sm) {
+// sorted descending, or -1 when the flag is set.  All 256 threads.
+__device__ __noinline__ int merge_runs(const uint64_t* runs, int nseg, int k, uint32_t* gh, const uint32_t* seqflag,
+                                       uint32_t* hist, uint32_t* cur, uint64_t* buf, SegSelSmem* sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t bad = __ldcg(seqflag);
     const int gm = static_cast<int>(__ldcg(gh + kGHistBins)) - 1;   // largest bin of any entry
-    if (gm < 0) return 0;
     if (tid == 0) {
         sm->bnd.bin = -1;
         sm->bnd.above = 0u;
+        sm->red[1] = static_cast<uint32_t>(gm);   // top of bin_order's range (all bins when not found below)
     }
-    // the 256 bins below the largest: thread t holds bin gm - 255 + t
-    {
-        const int bt = gm - (kWinBins - 1) + tid;
-        const uint32_t v = bt >= 0 ? __ldcg(gh + bt) : 0u;
-        uint32_t incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
-            if (lane + o < 32) incl += y;
-        }
-        if (lane == 0) sm->wcnt[warp] = incl;
-        __syncthreads();
-        uint32_t after = incl - v;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) after += q > warp ? sm->wcnt[q] : 0u;
-        const uint32_t kk = static_cast<uint32_t>(k);
-        if (after < kk && kk <= after + v) {
-            sm->bnd.bin = bt;
-            sm->bnd.above = after + v;   // entries at or above the bin
-        }
-        __syncthreads();
-    }
-    if (sm->bnd.bin < 0) {
-        // fewer than k entries in those bins: the suffix over all 8192 bins
-        // (thread t holds bins 32 t .. 32 t + 31)
-        uint32_t v[32];
+    if (bad == 0u && gm >= 0) {   // (the same in every thread)
+        // the 256 bins below the largest: thread t holds bin gm - 255 + t
         {
-            const uint4* g4 = reinterpret_cast<const uint4*>(gh) + 8 * tid;
+            const int bt = gm - (kWinBins - 1) + tid;
+            const uint32_t v = bt >= 0 ? __ldcg(gh + bt) : 0u;
+            uint32_t incl = v;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint4 x = __ldcg(g4 + j);
-                v[4 * j] = x.x;
-                v[4 * j + 1] = x.y;
-                v[4 * j + 2] = x.z;
-                v[4 * j + 3] = x.w;
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+                if (lane + o < 32) incl += y;
             }
+            if (lane == 0) sm->wcnt[warp] = incl;
+            __syncthreads();
+            uint32_t after = incl - v;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) after += q > warp ? sm->wcnt[q] : 0u;
+            const uint32_t kk = static_cast<uint32_t>(k);
+            if (after < kk && kk <= after + v) {
+                sm->bnd.bin = bt;
+                sm->bnd.above = after + v;   // entries at or above the bin
+            }
+            // the bin where the count from the top reaches min(16, k) (at or
+            // above the boundary bin, since that count is at most k)
+            const uint32_t kt = min(kk, 16u);
+            if (after < kt && kt <= after + v) sm->red[1] = static_cast<uint32_t>(bt);
+            __syncthreads();
         }
-        uint32_t sum = 0;
+        if (sm->bnd.bin < 0) {
+            // fewer than k entries in those bins: the suffix over all 8192 bins
+            // (thread t holds bins 32 t .. 32 t + 31)
+            uint32_t v[32];
+            {
+                const uint4* g4 = reinterpret_cast<const uint4*>(gh) + 8 * tid;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sum += v[j];
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
-            if (lane + o < 32) incl += y;
-        }
-        __syncthreads();
-        if (lane == 0) sm->wcnt[warp] = incl;
-        __syncthreads();
-        uint32_t after = incl - sum, total = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const uint32_t x = sm->wcnt[q];
-            after += q > warp ? x : 0u;
-            total += x;
-        }
-        const uint32_t kk = min(static_cast<uint32_t>(k), total);
-        if (kk > 0u && after < kk && kk <= after + sum) {
-            uint32_t acc = after;
-#pragma unroll
-            for (int j = 31; j >= 0; --j) {
-                if (acc < kk && kk <= acc + v[j]) {
-                    sm->bnd.bin = 32 * tid + j;
-                    sm->bnd.above = acc + v[j];
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 x = __ldcg(g4 + j);
+                    v[4 * j] = x.x;
+                    v[4 * j + 1] = x.y;
+                    v[4 * j + 2] = x.z;
+                    v[4 * j + 3] = x.w;
                 }
-                acc += v[j];
+            }
+            uint32_t sum = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sum += v[j];
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+                if (lane + o < 32) incl += y;
+            }
+            __syncthreads();
+            if (lane == 0) sm->wcnt[warp] = incl;
+            __syncthreads();
+            uint32_t after = incl - sum, total = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t x = sm->wcnt[q];
+                after += q > warp ? x : 0u;
+                total += x;
+            }
+            const uint32_t kk = min(static_cast<uint32_t>(k), total);
+            if (kk > 0u && after < kk && kk <= after + sum) {
+                uint32_t acc = after;
+#pragma unroll
+                for (int j = 31; j >= 0; --j) {
+                    if (acc < kk && kk <= acc + v[j]) {
+                        sm->bnd.bin = 32 * tid + j;
+                        sm->bnd.above = acc + v[j];
+                    }
+                    acc += v[j];
+                }
             }
         }
-        __syncthreads();
     }
+    // every read of gh is done: zero it (16-byte stores, nothing waits on them)
+    __syncthreads();
+    {
+        uint4* g4 = reinterpret_cast<uint4*>(gh);
+        for (int i = tid; i < kGHistWords / 4; i += kTopkThreads) g4[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (bad != 0u) return -1;
+    if (sm->bnd.bin < 0) return 0;
+    const int gtop = static_cast<int>(sm->red[1]);
     const int bstar = sm->bnd.bin;
     const uint32_t ncand = sm->bnd.above;
-    if (bstar < 0) return 0;
-    uint64_t* cand = buf + 2048;
     if (ncand <= 2048u && nseg == 2) {
+        uint64_t* cand = buf + 2048;
         // Two runs (a sequence of two segments): each run is sorted, so its
         // candidates (entries of bins >= bstar) are a prefix.  Find the two
         // prefix lengths, copy the prefixes next to each other and merge them
@@ -645,6 +658,7 @@ __device__ __noinline__ int merge_runs(const uint64_t* runs, int nseg, int k, co
         __syncthreads();
     }
     if (ncand <= 2048u) {
+        uint64_t* cand = buf;   // put in order in place, buf[2048, 4096) the scratch
         uint32_t* cnt = &sm->red[0];
         // open runs of a round: two lists of 128 in sm->scratch, used in turn
         if (tid == 0) {
@@ -654,65 +668,81 @@ __device__ __noinline__ int merge_runs(const uint64_t* runs, int nseg, int k, co
         }
         __syncthreads();
         const unsigned long long* rr = reinterpret_cast<const unsigned long long*>(runs);
-        auto append = [&](uint64_t c, bool t) {
-            const unsigned bal = __ballot_sync(0xffffffffu, t);
-            uint32_t base = 0u;
-            if (lane == 0 && bal != 0u) base = atomicAdd(cnt, static_cast<uint32_t>(__popc(bal)));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            const uint32_t pos = base + static_cast<uint32_t>(__popc(bal & ((1u << lane) - 1u)));
-            if (t && pos < 2048u) cand[pos] = c;
+        constexpr int U = 8;   // loads in flight per thread
+        // a round's length R = 2^lg: the largest power of two at most
+        // U * 256 / open, and at least 32 (entry f of a round is entry
+        // f & (R - 1) of open run f >> lg, no division)
+        auto round_lg = [&](int open) {
+            const int r = U * kTopkThreads / open;
+            return r < 32 ? 5 : 31 - __clz(static_cast<uint32_t>(r));
         };
-        auto round_len = [&](int open, int m) {
-            int r = ((4 * kTopkThreads / open) + 31) & ~31;
-            r = r < 32 ? 32 : r;
-            return r < k - m ? r : k - m;
-        };
-        // every run is open at first; an open run holds at least R candidates
-        // (R >= 32 or the run's end), so at most 64 stay open after a round
+        // every run is open at first; a run stays open only when all of the
+        // R >= 32 entries it gave are candidates, so at most 64 stay open
         int m = 0, nopen = nseg, li = 0;
         bool all = true;
-        int R = round_len(nseg, 0);
+        int lg = round_lg(nseg);
         while (true) {
+            const int R = 1 << lg;
+            const int rlen = min(R, k - m);   // entries read of each open run
             const int nflat = nopen * R;
             const uint32_t* cur_list = sm->scratch + 128 * li;
             uint32_t* next_list = sm->scratch + 128 * (li ^ 1);
             uint32_t* next_n = &sm->red[2 + (li ^ 1)];
-            for (int f0 = 0; f0 < nflat; f0 += 4 * kTopkThreads) {
-                uint64_t c[4];
-                int jr[4], e[4];
+            for (int f0 = 0; f0 < nflat; f0 += U * kTopkThreads) {
+                uint64_t c[U];
+                int jr[U], e[U];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < U; ++q) {
                     const int f = f0 + q * kTopkThreads + tid;
-                    const int jj = f / R;
-                    e[q] = f - jj * R;
-                    jr[q] = f < nflat ? (all ? jj : static_cast<int>(cur_list[jj])) : 0;
-                    c[q] = f < nflat ? static_cast<uint64_t>(__ldcg(rr + static_cast<int64_t>(jr[q]) * k + m + e[q]))
-                                     : 0ull;
+                    const int jj = f >> lg;
+                    e[q] = f & (R - 1);
+                    const bool in = f < nflat && e[q] < rlen;
+                    jr[q] = in ? (all ? jj : static_cast<int>(cur_list[jj])) : 0;
+                    c[q] = in ? static_cast<uint64_t>(__ldcg(rr + static_cast<int64_t>(jr[q]) * k + m + e[q])) : 0ull;
                 }
+                uint32_t mask = 0u;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < U; ++q) {
                     const bool t = c[q] != 0ull && static_cast<int>(win_bin(comp_key(c[q]))) >= bstar;
-                    append(c[q], t);
-                    if (t && e[q] == R - 1 && m + R < k) next_list[atomicAdd(next_n, 1u) & 127u] = static_cast<uint32_t>(jr[q]);
+                    mask |= t ? (1u << q) : 0u;
+                    if (t && e[q] == rlen - 1 && m + rlen < k)
+                        next_list[atomicAdd(next_n, 1u) & 127u] = static_cast<uint32_t>(jr[q]);
+                }
+                // the candidates appended with one shared atomic per warp
+                const uint32_t mine = static_cast<uint32_t>(__popc(mask));
+                uint32_t incl = mine;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                uint32_t base = 0u;
+                if (lane == 31 && incl != 0u) base = atomicAdd(cnt, incl);
+                uint32_t pos = __shfl_sync(0xffffffffu, base, 31) + incl - mine;
+#pragma unroll
+                for (int q = 0; q < U; ++q) {
+                    if ((mask >> q) & 1u) {
+                        if (pos < 2048u) cand[pos] = c[q];
+                        ++pos;
+                    }
                 }
             }
             __syncthreads();
             nopen = static_cast<int>(min(*next_n, 128u));
             if (nopen == 0) break;
             if (tid == 0) sm->red[2 + li] = 0u;   // the list read this round is written next
-            m += R;
+            m += rlen;
             li ^= 1;
             all = false;
-            R = round_len(nopen, m);
+            lg = round_lg(nopen);
             __syncthreads();
         }
         const int got = static_cast<int>(min(*cnt, 2048u));
-        // keys lie in [the boundary bin's floor, the top of the largest bin]
+        // keys from the boundary bin's floor; the range mapped runs to the top
+        // of gtop (at most 15 entries lie above it)
         const uint32_t lo = static_cast<uint32_t>(bstar) << kWinShift;
-        const uint32_t hi = static_cast<uint32_t>((static_cast<uint64_t>(gm + 1) << kWinShift) - 1u);
-        bin_order(cand, got, buf, lo, hi, hist, cur, sm);
-        for (int i = tid; i < got; i += kTopkThreads) buf[i] = cand[i];
-        __syncthreads();
+        const uint32_t hi = static_cast<uint32_t>((static_cast<uint64_t>(gtop + 1) << kWinShift) - 1u);
+        bin_order(cand, got, buf + 2048, lo, hi, hist, cur, sm);
         return min(k, got);
     }
     return seg_select(GCompSet{runs, nseg * k}, k, hist, buf, sm);
