@@ -458,14 +458,28 @@ __device__ __forceinline__ void rank_pool(const uint64_t* pool, int lo, int hi, 
             srt[atomicAdd(&scur[sub(y)], 1u)] = y;
         }
         __syncthreads();
-        for (int q = tid; q < len; q += kTopkThreads) {
-            const uint64_t y = srt[q];
+        // ranks inside a sub-bin: the same trip counts in a warp (to the
+        // warp's largest sub-bin), sub-bin mates read four at a time (a
+        // composite is never zero, so a zero past a sub-bin's end counts
+        // nothing)
+        for (int q0 = 0; q0 < len; q0 += kTopkThreads) {
+            const int q = q0 + tid;
+            const uint64_t y = q < len ? srt[q] : 0ull;
             const uint32_t u = sub(y);
-            const int en = static_cast<int>(scur[u]), st = en - static_cast<int>(scnt[u]);
+            const int en = static_cast<int>(scur[u]);
+            const int c = q < len ? static_cast<int>(scnt[u]) : 0;
+            const int st = en - c;
+            const int m = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(c));
             int fp = st;
-            for (int z = st; z < en; ++z) fp += srt[z] > y ? 1 : 0;
+            for (int z = 0; z < m; z += 4) {
+                const uint64_t t0 = z < c ? srt[st + z] : 0ull;
+                const uint64_t t1 = z + 1 < c ? srt[st + z + 1] : 0ull;
+                const uint64_t t2 = z + 2 < c ? srt[st + z + 2] : 0ull;
+                const uint64_t t3 = z + 3 < c ? srt[st + z + 3] : 0ull;
+                fp += (t0 > y ? 1 : 0) + (t1 > y ? 1 : 0) + (t2 > y ? 1 : 0) + (t3 > y ? 1 : 0);
+            }
             const int rk = s0 + fp;
-            if (rk >= lo && rk < hi && rk < nsel) emit(rk, y);
+            if (q < len && rk >= lo && rk < hi && rk < nsel) emit(rk, y);
         }
         __syncthreads();
     }
