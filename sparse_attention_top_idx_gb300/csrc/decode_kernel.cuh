@@ -899,11 +899,17 @@ __global__ void __maxnreg__(120) decode_kernel(const __grid_constant__ CUtensorM
                            p.out_slot ? p.out_slot + static_cast<int64_t>(b) * p.topk : nullptr);
         }
         // generic accesses of the stages come before the next unit's copies
-        // into them; this CTA is done with its receive areas
+        // into them; this CTA is done with its receive areas.  The arrive is
+        // relaxed: the barrier only has to keep the peers' next writes into
+        // the receive areas behind this CTA's reads of them, and every such
+        // read has returned its value before the block barrier above (the
+        // values were consumed: ranks, emitted outputs), so no memory ordering
+        // is needed and the arrive need not wait for the outputs' global
+        // stores to complete
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) DSAIDX_PHASE(it, 12);
-        cluster_arrive();
+        cluster_arrive_relaxed();
         // the next unit (drawn by rank 0 during this one); slot (it + 1) & 1 is
         // used every other unit, so this is its (it >> 1)-th use
         const bool uok =
