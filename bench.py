@@ -45,9 +45,9 @@ N_POOL_COPIES = 9
 # hash of the measured kernel's code (its translation unit and every header it
 # includes, comments left out) when they were taken; a stale hash reports null.
 NCU_TRAFFIC = {
-    ("decode", "99c41581aa9592a4"): 31445504 + 0,
-    ("longctx", "99c41581aa9592a4"): 277289216 + 2772480,
-    ("prefill", "1dd4133fc7337444"): 139604992 + 537155840,   # the scoring kernel
+    ("decode", "cd4902da1e770c88"): 31444992 + 0,
+    ("longctx", "cd4902da1e770c88"): 277246976 + 2784256,
+    ("prefill", "9a835175a16cef1b"): 139506432 + 536455936,   # the scoring kernel
 }
 KERNEL_TU = {"decode": "decode.cu", "longctx": "decode.cu", "prefill": "prefill.cu"}
 

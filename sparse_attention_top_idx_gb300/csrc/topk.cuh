@@ -39,12 +39,25 @@ struct Boundary {
 // Find the bin holding the need-th largest candidate of a histogram of nbins
 // (a multiple of 256) bins.  Called by all 256 threads; scratch holds >= 256
 // words.  Result in *out (shared), valid after the call for every thread.
+// Thread t sums bins per t .. per t + per - 1; with 4096 bins (16 a thread,
+// hist 16-byte aligned) it reads them as four 16-byte slots, each thread
+// starting at slot (t >> 1) & 3, so that eight consecutive threads hit
+// distinct banks (word-by-word, a warp's 32 threads hit two banks).
 __device__ __forceinline__ void block_find_suffix(const uint32_t* hist, int nbins, uint32_t need,
                                   uint32_t* scratch, Boundary* out) {
     const int tid = threadIdx.x;
     const int per = nbins / kTopkThreads;
     uint32_t s = 0;
-    for (int i = 0; i < per; ++i) s += hist[tid * per + i];
+    if (per == 16) {
+        const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 4 * tid;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 x = h4[(j + (tid >> 1)) & 3];
+            s += x.x + x.y + x.z + x.w;
+        }
+    } else {
+        for (int i = 0; i < per; ++i) s += hist[tid * per + i];
+    }
     scratch[tid] = s;
     __syncthreads();
     if (tid < 32) {
