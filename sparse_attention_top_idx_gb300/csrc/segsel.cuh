@@ -382,8 +382,7 @@ __device__ __noinline__ void bin_order(uint64_t* a, int n, uint64_t* tmp, uint32
 
 // Histogram windows of the decode selection: bins of the score key at
 // 1/16 octave (key >> 19: sign, exponent and 4 mantissa bits; 8192 bins over
-// all keys); a CTA's window is the 256
-// bins below its largest score.
+// all keys); a CTA's window is the 256 bins below its largest score.
 constexpr int kWinShift = 19;
 constexpr int kWinBins = 256;                        // bins of a window, ending at the chunk's largest
 constexpr int kWinHead = 4;                          // anchor bin, count, largest key, device-check flag
